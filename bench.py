@@ -1,0 +1,471 @@
+#!/usr/bin/env python3
+"""Benchmark of the fine-grained FP8 forward path on B300.
+
+One step = one pass of the path over one batch of the dense workload
+(attention-projection shape: M = 4096 tokens, N = K = 7168; activations
+N(0,1) with 0.1% outlier channels x100, weights N(0,0.02); bf16 in, bf16
+out): quantize the activations in 1x128 tiles, quantize the weights in
+128x128 blocks, then the block-scaled FP8 GEMM with FP32 promotion.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `value` is whole-job TFLOP/s (2*M*N*K per step per
+GPU) with inputs resident in HBM, CUDA-event timed on the launching stream,
+L2 flushed between steps; `e2e` is the same metric through the C ABI from
+pinned host buffers (host<->device copies inside the timed region).  Under
+torchrun every rank runs its own replica (weak scaling; no collective on the
+data path) and the slowest rank's time is used.  `--impl reference` times the
+CPU oracle on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "dense"
+METRIC = ("block-scaled FP8 GEMM TFLOP/s and % dense FP8 peak; "
+          "quantizer GB/s and % HBM peak")
+# Dense FP8 peak = measured bf16 peak x the nominal fp8/bf16 ratio (4.5/2.25).
+FP8_OVER_BF16 = 2.0
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM traffic of one GEMM launch on the dense workload from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# source it was taken on; None until captured.
+TRAFFIC = {"gemm": None}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "fp8_common.cuh"):
+        with open(os.path.join(ROOT, "fp8_fine_grained_18_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, torch_device):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            try:
+                import torch
+                bus = torch.cuda.get_device_properties(torch_device).pci_bus_id
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(torch_device)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+
+    def _run(self):
+        nv = self.nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def algorithmic_bytes_q1(M, K):
+    return M * K * 3 + 4 * M * (K // 128)
+
+
+def algorithmic_bytes_q2(N, K, transposed=False):
+    return N * K * (4 if transposed else 3) + 4 * (N // 128) * (K // 128) * (2 if transposed else 1)
+
+
+def algorithmic_bytes_q3(M, K):
+    return M * K * 2 + 2 * 4 * M * (K // 128)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import fp8_fine_grained_18_b300 as fp8bs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks, peak_kind = load_peaks()
+
+    w = synth.WORKLOADS[WORKLOAD]
+    M, N, K = w.M, w.N, w.K
+    inp = synth.make_inputs(WORKLOAD)
+    a_host = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16)
+    b_host = torch.from_numpy(inp["B"].view(np.int16)).view(torch.bfloat16)
+    a = a_host.to(dev)
+    b = b_host.to(dev)
+    qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sb = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 126 MB L2
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fp8bs.quant_act_1x128(a, q=qa, scales=sa)
+        fp8bs.quant_weight_128x128(b, q=qb, scales=sb)
+        fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=c)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fp8bs.get_device_error(dev) != fp8bs.OK:
+        raise RuntimeError("device error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    wall0 = time.perf_counter()
+    with sampler:
+        for i in range(args.steps):
+            flush.zero_()
+            e = ev[i]
+            e[0].record(stream)
+            fp8bs.quant_act_1x128(a, q=qa, scales=sa)
+            e[1].record(stream)
+            fp8bs.quant_weight_128x128(b, q=qb, scales=sb)
+            e[2].record(stream)
+            fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=c)
+            e[3].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    if fp8bs.get_device_error(dev) != fp8bs.OK:
+        raise RuntimeError("device error in the timed region")
+    t_q1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    t_q2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    t_g = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    total_ms = sum(t_step)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = 2.0 * M * N * K
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # roofline of the dominant kernel (the GEMM)
+    g_ms = statistics.mean(t_g)
+    g_tflops = flops / (g_ms * 1e-3) / 1e12
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    traffic = None
+    tr = TRAFFIC.get("gemm")
+    if tr and tr.get("src_sha") == kernel_source_sha():
+        traffic = tr["bytes"]
+    roofline = {"bound": "tensor", "kernel": "gemm (block-scaled FP8, promoted)",
+                "achieved": round(g_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                "frac": round(g_tflops / fp8_peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} "
+                               "(fp8/bf16 nominal ratio)",
+                "frac_of_sustained": round(g_tflops / (peaks["bf16_tflops_sustained"] * FP8_OVER_BF16), 4),
+                "algorithmic_flops_per_launch": flops}
+    hbm = peaks["hbm_gbs"]
+    q1_gbs = algorithmic_bytes_q1(M, K) / (statistics.mean(t_q1) * 1e-3) / 1e9
+    q2_gbs = algorithmic_bytes_q2(N, K) / (statistics.mean(t_q2) * 1e-3) / 1e9
+    kernels = {
+        "quant_act_1x128": {"ms": round(statistics.mean(t_q1), 4), "GB/s": round(q1_gbs, 1),
+                            "frac_hbm": round(q1_gbs / hbm, 4)},
+        "quant_weight_128x128": {"ms": round(statistics.mean(t_q2), 4), "GB/s": round(q2_gbs, 1),
+                                 "frac_hbm": round(q2_gbs / hbm, 4)},
+        "gemm": {"ms": round(g_ms, 4), "TFLOP/s": round(g_tflops, 1),
+                 "frac_fp8_peak": round(g_tflops / fp8_peak, 4)},
+    }
+
+    # end to end through the C ABI from pinned host buffers
+    a_pin = a_host.pin_memory()
+    b_pin = b_host.pin_memory()
+    c_pin = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        a.copy_(a_pin, non_blocking=True); b.copy_(b_pin, non_blocking=True)
+        step(); c_pin.copy_(c, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        a.copy_(a_pin, non_blocking=True)
+        b.copy_(b_pin, non_blocking=True)
+        step()
+        c_pin.copy_(c, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": a.numel() * 2 + b.numel() * 2,
+           "d2h_bytes_per_step": c.numel() * 2, "ms_per_step": round(e2e_ms, 3)}
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": "dense attention-projection Fprop: quantize A 1x128 + W 128x128, "
+                               "block-scaled FP8 GEMM, bf16 out",
+                   "M": M, "N": N, "K": K, "seed": w.seed,
+                   "l2": "flushed between steps (256 MB write, outside the timed events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "kernels": kernels, "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(), "wall_timed_s": round(wall, 4),
+    }
+    if args.rows and rank == 0:
+        out["rows"] = measure_rows(fp8bs, torch, dev, peaks)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(M, N, K, inp, budget_s=20.0)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def _time_ms(fn, torch, iters=10, flush=None):
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(iters):
+        if flush is not None:
+            flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e))
+    return statistics.median(ts)
+
+
+def measure_rows(fp8bs, torch, dev, peaks):
+    """Every hot-path row at its own workload: quantizer GB/s, GEMM TFLOP/s."""
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    rows = {}
+
+    def bf(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def gemm_row(name, qa, sa, qb, sb, bkind, out_dtype, promote=True):
+        M, K = qa.shape
+        N = qb.shape[0]
+        c = torch.empty((M, N), dtype=out_dtype, device=dev)
+        ms = _time_ms(lambda: fp8bs.gemm(qa, sa, qb, sb, bkind, out_dtype=out_dtype, out=c,
+                                         promote=promote), torch, flush=flush)
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        rows[name] = {"M": M, "N": N, "K": K, "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                      "frac_fp8_peak": round(tf / fp8_peak, 4)}
+
+    def quant_row(name, fn, nbytes):
+        ms = _time_ms(fn, torch, flush=flush)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+
+    # MoE up/gate shape
+    moe = synth.make_inputs("moe")
+    a, b = bf(moe["A"]), bf(moe["B"])
+    qa, sa = fp8bs.quant_act_1x128(a)
+    qb, sb = fp8bs.quant_weight_128x128(b)
+    quant_row("Q1 moe A 8192x7168", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
+              algorithmic_bytes_q1(8192, 7168))
+    gemm_row("G1 moe 8192x4096x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
+    del a, b, qa, sa, qb, sb
+
+    # backward chain
+    bwd = synth.make_inputs("bwd")
+    x, wt, dy = bf(bwd["X"]), bf(bwd["W"]), bf(bwd["dY"])
+    qx, sx = fp8bs.quant_act_1x128(x)
+    qxT, sxT = fp8bs.requant_1x128_to_128x1(qx, sx)
+    quant_row("Q3 requant X 4096x2048", lambda: fp8bs.requant_1x128_to_128x1(qx, sx, qT=qxT, scalesT=sxT),
+              algorithmic_bytes_q3(4096, 2048))
+    qdyT, sdyT = fp8bs.quant_act_1x128(dy, transpose_out=True)
+    quant_row("Q1T dY 4096x7168 (128x1, transposed out)",
+              lambda: fp8bs.quant_act_1x128(dy, transpose_out=True, q=qdyT, scales=sdyT),
+              algorithmic_bytes_q1(4096, 7168))
+    qdy, sdy = fp8bs.quant_act_1x128(dy)
+    qw, sw, qwT, swT = fp8bs.quant_weight_128x128(wt, transposed=True)
+    quant_row("Q2+T W 7168x2048 (with transposed copy)",
+              lambda: fp8bs.quant_weight_128x128(wt, transposed=True, q=qw, scales=sw, qT=qwT, scalesT=swT),
+              algorithmic_bytes_q2(7168, 2048, transposed=True))
+    gemm_row("G1 dgrad 4096x2048x7168 bf16", qdy, sdy, qwT, swT, 0, torch.bfloat16)
+    gemm_row("G1 wgrad 7168x2048x4096 f32 (1x128 B scales)", qdyT, sdyT, qxT, sxT, 1, torch.float32)
+    del x, wt, dy, qx, sx, qxT, sxT, qdyT, sdyT, qdy, sdy, qw, sw, qwT, swT
+
+    # large-K stress, promoted and un-promoted
+    st = synth.make_inputs("stress")
+    a, b = bf(st["A"]), bf(st["B"])
+    del st
+    qa, sa = fp8bs.quant_act_1x128(a)
+    qb, sb = fp8bs.quant_act_1x128(b)
+    quant_row("Q1 stress A 8192x16384", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
+              algorithmic_bytes_q1(8192, 16384))
+    gemm_row("G1 stress 8192x8192x16384 f32", qa, sa, qb, sb, 1, torch.float32)
+    gemm_row("G2 un-promoted stress 8192x8192x16384 f32", qa, sa, qb, sb, 1, torch.float32,
+             promote=False)
+    return rows
+
+
+def cpu_baseline(M, N, K, inp, budget_s=20.0):
+    """The oracle, as it stands, on a bounded sample of the step's workload."""
+    import oracle
+    oracle.lib()
+    m_s = 32
+    w_rows = 128
+    t0 = time.perf_counter()
+    qa, sa = oracle.quant_act_1x128(inp["A"][:m_s])
+    qw_part, _ = oracle.quant_weight_128x128(inp["B"][:w_rows])
+    t1 = time.perf_counter()
+    # GEMM rows need the full quantized weight; its quantization is counted
+    # above only for the sampled share (w_rows of N rows)
+    qw, sw = oracle.quant_weight_128x128(inp["B"])
+    t2 = time.perf_counter()
+    ms = np.repeat(np.arange(m_s), N)
+    ns = np.tile(np.arange(N), m_s)
+    oracle.gemm_sampled(qa, sa, qw, sw, oracle.BSCALE_BLOCK_128x128, ms, ns)
+    t3 = time.perf_counter()
+    secs = (t1 - t0) + (t3 - t2)
+    return {"value": round(2.0 * m_s * N * K / secs / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{m_s} of {M} activation rows: quantize them (1x128), quantize {w_rows} of "
+                      f"{N} weight rows (128x128), and the {m_s}x{N}x{K} GEMM in double "
+                      f"({secs:.1f} s of CPU time)"}
+
+
+# ------------------------------------------------------- reference arm (CPU)
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    w = synth.WORKLOADS[WORKLOAD]
+    M, N, K = w.M, w.N, w.K
+    inp = synth.make_inputs(WORKLOAD)
+    qw, sw = oracle.quant_weight_128x128(inp["B"])
+    # size one step so that warm-up + steps take about 90 s in total
+    probe_rows = 2
+    t0 = time.perf_counter()
+    _ref_step(oracle, inp, qw, sw, 0, probe_rows, N, K)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(M, budget / max(per_row, 1e-9))))
+    for i in range(args.warmup):
+        _ref_step(oracle, inp, qw, sw, i * rows % M, rows, N, K)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _ref_step(oracle, inp, qw, sw, (i * rows) % max(1, M - rows), rows, N, K)
+    secs = time.perf_counter() - t0
+    value = 2.0 * rows * N * K * args.steps / secs / 1e12
+    sample = (f"each step: {rows} of {M} activation rows quantized (1x128) and their "
+              f"{rows}x{N}x{K} GEMM in double against the weight quantized once (128x128)")
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+           "config": {"workload": "dense attention-projection Fprop (CPU oracle sample)",
+                      "M": M, "N": N, "K": K, "seed": w.seed},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                            "cores": oracle.num_threads(), "sample": sample},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def _ref_step(oracle, inp, qw, sw, r0, rows, N, K):
+    qa, sa = oracle.quant_act_1x128(inp["A"][r0:r0 + rows])
+    ms = np.repeat(np.arange(rows), N)
+    ns = np.tile(np.arange(N), rows)
+    return oracle.gemm_sampled(qa, sa, qw, sw, oracle.BSCALE_BLOCK_128x128, ms, ns)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rows", type=int, default=1, help="also time every hot-path row (1/0)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

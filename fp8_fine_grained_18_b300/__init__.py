@@ -1,0 +1,163 @@
+"""Python binding of libfp8bs: fine-grained FP8 quantization and the
+block-scaled FP8 GEMM on B300 (sm_103a).
+
+Argument marshalling only.  Every call goes through the C ABI declared in
+include/fp8bs.h (loaded with ctypes from libfp8bs.so next to this file);
+PyTorch supplies device memory and the current CUDA stream.  There is no
+fallback: if the library is missing, importing this package fails.
+
+Layouts (see include/fp8bs.h): codes are uint8 tensors holding E4M3 bits;
+1x128-group scales of X[rows][cols] are float32 [cols/128, rows]; weight
+block scales of W[N][K] are float32 [N/128, K/128].
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
+OUT_BF16, OUT_F32 = 0, 1
+BSCALE_BLOCK_128x128, BSCALE_TILE_1x128 = 0, 1
+GROUP = 128
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libfp8bs.so is not built ({LIB_PATH}); run "
+                      "`python -m fp8_fine_grained_18_b300.build`")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+
+_SIGS = {
+    "fp8bs_quant_act_1x128": [_P, _I64, _I64, _I, _P, _P, _P],
+    "fp8bs_quant_weight_128x128": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "fp8bs_requant_1x128_to_128x1": [_P, _P, _I64, _I64, _P, _P, _P],
+    "fp8bs_gemm": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P],
+    "fp8bs_gemm_ex": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _P],
+    "fp8bs_debug_gemm_stall": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I, _P],
+    "fp8bs_get_device_error": [_P],
+    "fp8bs_status_string": [_I],
+    "fp8bs_last_cuda_error": [],
+    "fp8bs_version": [],
+}
+for _name, _args in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_char_p if _name == "fp8bs_status_string" else ctypes.c_int
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib.fp8bs_status_string(status).decode()
+        if status == ERR_CUDA:
+            msg += f" (cudaError {_lib.fp8bs_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+def lib():
+    """The raw ctypes handle of libfp8bs.so."""
+    return _lib
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise Fp8bsError(status, where)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _empty(shape, dtype, like):
+    return torch.empty(shape, dtype=dtype, device=like.device)
+
+
+def quant_act_1x128(x: torch.Tensor, transpose_out: bool = False, q=None, scales=None):
+    """bf16 x[M, K] -> (codes uint8, scales float32).
+
+    transpose_out=False: codes [M, K], scales [K/128, M] (1x128 tiles).
+    transpose_out=True:  codes [K, M], scales [M/128, K] (128x1 tiles of x,
+    i.e. 1x128 tiles of x transposed).
+    """
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    M, K = x.shape
+    if transpose_out:
+        q = _empty((K, M), torch.uint8, x) if q is None else q
+        scales = _empty((M // GROUP, K), torch.float32, x) if scales is None else scales
+    else:
+        q = _empty((M, K), torch.uint8, x) if q is None else q
+        scales = _empty((K // GROUP, M), torch.float32, x) if scales is None else scales
+    _check(_lib.fp8bs_quant_act_1x128(_ptr(x), M, K, int(transpose_out), _ptr(q), _ptr(scales),
+                                      _stream(x)), "fp8bs_quant_act_1x128")
+    return q, scales
+
+
+def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, q=None, scales=None,
+                         qT=None, scalesT=None):
+    """bf16 w[N, K] -> (codes [N, K], scales [N/128, K/128]) and, with
+    transposed=True, also (codesT [K, N], scalesT [K/128, N/128])."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.is_contiguous()
+    N, K = w.shape
+    q = _empty((N, K), torch.uint8, w) if q is None else q
+    scales = _empty((N // GROUP, K // GROUP), torch.float32, w) if scales is None else scales
+    if transposed:
+        qT = _empty((K, N), torch.uint8, w) if qT is None else qT
+        scalesT = _empty((K // GROUP, N // GROUP), torch.float32, w) if scalesT is None else scalesT
+    _check(_lib.fp8bs_quant_weight_128x128(_ptr(w), N, K, _ptr(q), _ptr(scales),
+                                           _ptr(qT if transposed else None),
+                                           _ptr(scalesT if transposed else None), _stream(w)),
+           "fp8bs_quant_weight_128x128")
+    return (q, scales, qT, scalesT) if transposed else (q, scales)
+
+
+def requant_1x128_to_128x1(q: torch.Tensor, scales: torch.Tensor, qT=None, scalesT=None):
+    """codes q[M, K] with scales [K/128, M] -> (qT [K, M], scalesT [M/128, K])."""
+    assert q.dtype == torch.uint8 and scales.dtype == torch.float32
+    M, K = q.shape
+    qT = _empty((K, M), torch.uint8, q) if qT is None else qT
+    scalesT = _empty((M // GROUP, K), torch.float32, q) if scalesT is None else scalesT
+    _check(_lib.fp8bs_requant_1x128_to_128x1(_ptr(q), _ptr(scales), M, K, _ptr(qT), _ptr(scalesT),
+                                             _stream(q)), "fp8bs_requant_1x128_to_128x1")
+    return qT, scalesT
+
+
+def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
+         bkind: int = BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, promote: bool = True,
+         out=None):
+    """C[M, N] = block-scaled a[M, K] * b[N, K]^T (bf16 or float32 out)."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8
+    M, K = a.shape
+    N = b.shape[0]
+    odt = OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32
+    c = _empty((M, N), out_dtype, a) if out is None else out
+    _check(_lib.fp8bs_gemm_ex(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K, _ptr(c),
+                              odt, int(bool(promote)), _stream(a)), "fp8bs_gemm")
+    return c
+
+
+def debug_gemm_stall(a, sa, b, sb, skip_iter: int, out=None):
+    """Test support: see fp8bs_debug_gemm_stall in include/fp8bs.h."""
+    M, K = a.shape
+    N = b.shape[0]
+    c = _empty((M, N), torch.float32, a) if out is None else out
+    _check(_lib.fp8bs_debug_gemm_stall(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, _ptr(c),
+                                       int(skip_iter), _stream(a)), "fp8bs_debug_gemm_stall")
+    return c
+
+
+def get_device_error(device=None) -> int:
+    """Synchronizes the current stream; returns OK or ERR_TIMEOUT (and clears it)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    s = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    return _lib.fp8bs_get_device_error(s)
+
+
+def version() -> int:
+    return _lib.fp8bs_version()

@@ -1,0 +1,181 @@
+// api.cu -- the exported C ABI of libfp8bs (declared in include/fp8bs.h):
+// host-side argument validation, device-architecture check, and dispatch to
+// the kernel launchers.  Nothing is launched when an argument is invalid.
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fp8bs.h"
+#include "launch.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fp8bs_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return FP8BS_OK;
+  t_last_cuda_error = (int)e;
+  return FP8BS_ERR_CUDA;
+}
+
+// 0 = unknown, 1 = sm_103, 2 = other
+int g_arch_cache[128];
+
+fp8bs_status check_device() {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(e);
+  }
+  int cached = (dev >= 0 && dev < 128) ? g_arch_cache[dev] : 0;
+  if (cached == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      return cuda_status(cudaGetLastError());
+    }
+    cached = (major == 10 && minor == 3) ? 1 : 2;
+    if (dev >= 0 && dev < 128) g_arch_cache[dev] = cached;
+  }
+  return cached == 1 ? FP8BS_OK : FP8BS_ERR_ARCH;
+}
+
+cudaStream_t as_cuda(fp8bs_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;  // kernels index rows with int32
+
+fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                         fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
+                         fp8bs_out_dtype out, int promote, int skip_iter, fp8bs_stream_t stream) {
+  if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (bkind != FP8BS_BSCALE_BLOCK_128x128 && bkind != FP8BS_BSCALE_TILE_1x128)
+    return FP8BS_ERR_INVALID_ARG;
+  if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+  if (promote != 0 && promote != 1) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FP8BS_OK;
+  if (!a || !sa || !b || !sb || !c) return FP8BS_ERR_INVALID_ARG;
+  if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(c))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  fp8bs::GemmArgs g;
+  g.a = a;
+  g.sa = sa;
+  g.b = b;
+  g.sb = sb;
+  g.b_tile = bkind == FP8BS_BSCALE_TILE_1x128;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.c = c;
+  g.out_bf16 = out == FP8BS_OUT_BF16;
+  g.promote = promote != 0;
+  g.skip_iter = skip_iter;
+  return cuda_status(fp8bs::launch_gemm(g, as_cuda(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8bs_status fp8bs_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, int transpose_out,
+                                   uint8_t* q, float* scales, fp8bs_stream_t stream) {
+  if (M < 0 || K < 0 || (transpose_out != 0 && transpose_out != 1)) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (!x_bf16 || !q || !scales) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0 || (transpose_out && M % 128 != 0)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (K / 128 > 65535 || (transpose_out && M / 128 > 65535) || M >= kMaxDim * 64)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales)) return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  cudaError_t e = transpose_out
+                      ? fp8bs::launch_quant_act_128x1(x_bf16, M, K, q, scales, as_cuda(stream))
+                      : fp8bs::launch_quant_act_1x128(x_bf16, M, K, q, scales, as_cuda(stream));
+  return cuda_status(e);
+}
+
+fp8bs_status fp8bs_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, uint8_t* q,
+                                        float* scales, uint8_t* qT, float* scalesT,
+                                        fp8bs_stream_t stream) {
+  if (N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if ((qT == nullptr) != (scalesT == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (N == 0 || K == 0) return FP8BS_OK;
+  if (!w_bf16 || !q || !scales) return FP8BS_ERR_INVALID_ARG;
+  if (N % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (N / 128 > 65535 || K / 128 > (int64_t)1 << 30) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w_bf16) || !aligned16(q) || !aligned16(scales) || (qT && !aligned16(qT)) ||
+      (scalesT && !aligned16(scalesT)))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(
+      fp8bs::launch_quant_weight_128x128(w_bf16, N, K, q, scales, qT, scalesT, as_cuda(stream)));
+}
+
+fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t* q, const float* scales, int64_t M,
+                                          int64_t K, uint8_t* qT, float* scalesT,
+                                          fp8bs_stream_t stream) {
+  if (M < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (!q || !scales || !qT || !scalesT) return FP8BS_ERR_INVALID_ARG;
+  if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (M / 128 > 65535 || K / 128 > (int64_t)1 << 30) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(q) || !aligned16(scales) || !aligned16(qT) || !aligned16(scalesT))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(
+      fp8bs::launch_requant_1x128_to_128x1(q, scales, M, K, qT, scalesT, as_cuda(stream)));
+}
+
+fp8bs_status fp8bs_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                        fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
+                        fp8bs_out_dtype out, fp8bs_stream_t stream) {
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, 1, -1, stream);
+}
+
+fp8bs_status fp8bs_gemm_ex(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
+                           fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
+                           fp8bs_out_dtype out, int promote, fp8bs_stream_t stream) {
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, promote, -1, stream);
+}
+
+fp8bs_status fp8bs_debug_gemm_stall(const uint8_t* a, const float* sa, const uint8_t* b,
+                                    const float* sb, int64_t M, int64_t N, int64_t K, void* c,
+                                    int skip_iter, fp8bs_stream_t stream) {
+  if (skip_iter < 0) return FP8BS_ERR_INVALID_ARG;
+  return gemm_common(a, sa, b, sb, FP8BS_BSCALE_BLOCK_128x128, M, N, K, c, FP8BS_OUT_F32, 1,
+                     skip_iter, stream);
+}
+
+const char* fp8bs_status_string(fp8bs_status s) {
+  switch (s) {
+    case FP8BS_OK: return "ok";
+    case FP8BS_ERR_INVALID_ARG: return "invalid argument";
+    case FP8BS_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case FP8BS_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FP8BS_ERR_ARCH: return "device is not sm_103 (B300)";
+    case FP8BS_ERR_CUDA: return "CUDA error";
+    case FP8BS_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+fp8bs_status fp8bs_get_device_error(fp8bs_stream_t stream) {
+  unsigned int word = 0;
+  cudaError_t e = fp8bs::read_and_clear_device_error(as_cuda(stream), &word);
+  if (e != cudaSuccess) return cuda_status(e);
+  return word ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
+}
+
+int fp8bs_last_cuda_error(void) { return t_last_cuda_error; }
+
+int fp8bs_version(void) { return 100; }
+
+}  // extern "C"

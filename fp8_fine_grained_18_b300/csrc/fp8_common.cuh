@@ -1,0 +1,96 @@
+// fp8_common.cuh -- device helpers shared by the libfp8bs kernels:
+// bf16 unpacking, E4M3 packing/unpacking through the hardware converters,
+// and the per-group scale and quotient arithmetic of the quantizers.
+//
+// Quantization rule (one group = a 1x128 tile, a 128x1 tile or a 128x128
+// block; DeepSeek-V3 fine-grained quantization, page P1 paragraph 3):
+//   amax = max |x| over the group (NaN ignored, Inf included)
+//   s    = fl32(amax / 448)                      (one IEEE division)
+//   code = E4M3_RNE_satfinite(fl32(x / s))       (two roundings)
+//   s == 0      -> every non-NaN element codes as a zero of its own sign
+//   NaN element -> 0x7F
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+constexpr int kGroup = 128;          // 1x128 tiles, 128x128 blocks
+constexpr float kE4M3Max = 448.0f;   // largest finite E4M3FN value
+// Below this scale the reciprocal-based quotient can meet FP32 subnormals;
+// such groups take the exact-division path.
+constexpr float kFastScaleMin = 0x1.0p-92f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two floats -> two E4M3 codes (RNE, saturate to +-448); lo in byte 0.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two E4M3 codes (byte 0 = first) -> two exact floats.
+__device__ __forceinline__ float2 e4m3x2_decode(uint32_t two_codes) {
+  uint32_t h2;
+  uint16_t in = (uint16_t)two_codes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(in));
+  float lo, hi;
+  asm("{.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;}"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+  return make_float2(lo, hi);
+}
+
+// Scale of a group whose max magnitude is amax.
+__device__ __forceinline__ float group_scale(float amax) { return __fdiv_rn(amax, kE4M3Max); }
+
+// Fast path: a normal, finite scale.  r must be the correctly rounded
+// reciprocal of s.  One Markstein correction step (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", 1990):
+// q0 = x*r, e = x - s*q0 (exact), q = q0 + e*r, each rounded once.  For the
+// bf16 inputs of the activation and weight quantizers it reproduces the IEEE
+// quotient fl32(x/s) wherever the quotient is >= 2^-12 (checked exhaustively
+// over all bf16 significand pairs and exponent gaps); below that every
+// candidate codes as a signed zero.
+// The correction adds a zero of either sign for x = +-0 and may produce +0
+// for a negative quotient that underflows, so x's sign is put back: for a
+// positive scale the quotient's sign is always x's sign.
+__device__ __forceinline__ float with_sign_of(float q, float x) {
+  return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+__device__ __forceinline__ float quotient_1step(float x, float s, float r) {
+  float q0 = __fmul_rn(x, r);
+  float e = __fmaf_rn(-q0, s, x);
+  return with_sign_of(__fmaf_rn(e, r, q0), x);
+}
+
+// Two correction steps: the first makes the quotient faithful for any FP32
+// x, the second then yields the correctly rounded quotient (Markstein's
+// theorem).  Used where x is a full 24-bit FP32 value (the requantizer).
+__device__ __forceinline__ float quotient_2step(float x, float s, float r) {
+  float q0 = __fmul_rn(x, r);
+  float e0 = __fmaf_rn(-q0, s, x);
+  float q1 = __fmaf_rn(e0, r, q0);
+  float e1 = __fmaf_rn(-q1, s, x);
+  return with_sign_of(__fmaf_rn(e1, r, q1), x);
+}
+
+// General path for one element: exact division and every special case.
+__device__ __forceinline__ float quotient_general(float x, float s) {
+  if (x != x) return x;  // NaN stays NaN
+  if (s == 0.0f) return __uint_as_float(__float_as_uint(x) & 0x80000000u);
+  return __fdiv_rn(x, s);
+}
+
+// Codes of two quotients with NaN -> 0x7F made explicit.
+__device__ __forceinline__ uint32_t e4m3x2_nan(float lo, float hi) {
+  uint32_t c = e4m3x2(lo, hi);
+  if (lo != lo) c = (c & 0xFF00u) | 0x7Fu;
+  if (hi != hi) c = (c & 0x00FFu) | 0x7F00u;
+  return c;
+}
+
+}  // namespace fp8bs

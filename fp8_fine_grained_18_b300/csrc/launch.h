@@ -1,0 +1,38 @@
+// launch.h -- internal host-side launchers of the libfp8bs kernels.  The
+// exported C ABI (include/fp8bs.h) validates arguments and calls these.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
+                                   cudaStream_t stream);
+cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t* qT, float* sT,
+                                   cudaStream_t stream);
+cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
+                                        uint8_t* qT, float* sT, cudaStream_t stream);
+cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
+                                          uint8_t* qT, float* sT, cudaStream_t stream);
+
+struct GemmArgs {
+  const uint8_t* a;
+  const float* sa;
+  const uint8_t* b;
+  const float* sb;
+  bool b_tile;  // B scales per 1x128 tile (else per 128x128 block)
+  int64_t M, N, K;
+  void* c;
+  bool out_bf16;
+  bool promote;
+  int skip_iter;  // test hook: producer skips this pipeline iteration (-1: never)
+};
+
+cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+// Reads and clears the device error word of the GEMM's bounded waits
+// (synchronizes the stream first).  *word = 0 when nothing timed out.
+cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
+
+}  // namespace fp8bs

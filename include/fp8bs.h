@@ -1,0 +1,192 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs: fine-grained FP8 quantization and the
+ * block-scaled FP8 GEMM that consumes it, for NVIDIA B300 (sm_103a).
+ *
+ * The method (DeepSeek-V3 FP8 training, as quoted by the five scraped pages
+ * cited below as P1..P5 with their paragraphs as ¶n):
+ *   - activations get one FP32 scale per 1x128 tile and weights one per
+ *     128x128 block, each derived online from the tile's maximum absolute
+ *     value, then cast to FP8 [P1¶3];
+ *   - the scales run along the inner dimension K and are multiplied in on
+ *     the CUDA cores while dequantizing [P1¶2], with partial sums promoted
+ *     into FP32 because tensor-core accumulation alone is limited to about
+ *     14 bits [P1¶3][P1¶4][P2¶3];
+ *   - cached activations are re-tiled from 1x128 to 128x1 for the backward
+ *     pass [P1¶3];
+ *   - the GEMMs take FP8 inputs and write BF16 or FP32 [P4¶4].
+ * Page key: P1 = xn--9g3bo1gtkw0l8ubf92bgle.kr qna wr_id=32373,
+ * P2 = why-be.why-be.co.kr as_center wr_id=73620,
+ * P3 = xn--9g3bo1gtkw0l8ubf92bgle.kr qna wr_id=113503,
+ * P4 = bestpmk.kr free wr_id=299512.
+ *
+ * Readings where the pages are silent: FP8 = OCP E4M3FN (max 448, NaN
+ * 0x7F/0xFF, no infinity); scale s = fl32(amax / 448); code =
+ * E4M3_round_nearest_even_satfinite(fl32(x / s)); amax ignores NaN and
+ * includes Inf; an all-zero tile has s = 0 and signed-zero codes; a NaN
+ * element codes as 0x7F; promotion happens once per 128-wide K group.
+ *
+ * Conventions for every call:
+ *   - All pointers are DEVICE pointers, 16-byte aligned, dense row-major,
+ *     owned and allocated by the caller, and must stay valid until the work
+ *     queued on `stream` finishes.  The library allocates no per-call
+ *     memory; outputs must not alias inputs.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and may be issued from several host threads on
+ *     different streams.
+ *   - Argument errors are detected on the host before anything is launched
+ *     and returned synchronously; no output is touched in that case.
+ *   - FP8BS_ERR_CUDA reports a failed CUDA call (the cudaError_t value is
+ *     kept per host thread, see fp8bs_last_cuda_error()).
+ *   - Scale layout for 1x128 groups of an operand X[rows][cols]:
+ *     s[cols/128][rows] (FP32, rows contiguous).  Weight blocks of W[N][K]:
+ *     s[N/128][K/128].
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, without requiring the CUDA headers. */
+typedef struct CUstream_st *fp8bs_stream_t;
+
+typedef enum {
+  FP8BS_OK = 0,
+  FP8BS_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum */
+  FP8BS_ERR_UNSUPPORTED_SHAPE = 2, /* a size that is not a required multiple */
+  FP8BS_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned */
+  FP8BS_ERR_ARCH = 4,              /* current device is not sm_103 */
+  FP8BS_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
+  FP8BS_ERR_TIMEOUT = 6            /* a bounded device wait gave up */
+} fp8bs_status;
+
+typedef enum { FP8BS_OUT_BF16 = 0, FP8BS_OUT_F32 = 1 } fp8bs_out_dtype;
+
+typedef enum {
+  /* B scales per 128x128 block: sb[N/128][K/128] (forward, input-grad) */
+  FP8BS_BSCALE_BLOCK_128x128 = 0,
+  /* B scales per 1x128 tile of each B row: sb[K/128][N] (weight-grad, whose
+   * B operand is an activation re-tiled along tokens) */
+  FP8BS_BSCALE_TILE_1x128 = 1
+} fp8bs_bscale_kind;
+
+/*
+ * Activation quantizer [P1¶3]: one scale per 1x128 tile, from the tile's
+ * online max-abs value.
+ *
+ * transpose_out == 0:
+ *   x: bf16 [M][K] -> q: E4M3 [M][K], scales: f32 [K/128][M].
+ *   Requires K % 128 == 0; M >= 0 (any M, including a ragged tail).
+ * transpose_out == 1 (128x1 tiles for the weight-gradient GEMM, [P1¶3]):
+ *   x: bf16 [M][K] -> q: E4M3 [K][M] (x transposed), scales: f32 [M/128][K]:
+ *   the result equals mode 0 applied to the transpose of x.
+ *   Requires M % 128 == 0 and K % 128 == 0.
+ * M == 0 or K == 0 is a no-op returning FP8BS_OK.
+ */
+fp8bs_status fp8bs_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K,
+                                   int transpose_out, uint8_t *q,
+                                   float *scales, fp8bs_stream_t stream);
+
+/*
+ * Weight quantizer [P1¶3]: one scale per 128x128 block of W.
+ *   w: bf16 [N][K] -> q: E4M3 [N][K], scales: f32 [N/128][K/128].
+ *   qT (nullable): E4M3 [K][N], the same codes transposed (the K-major B
+ *   operand of the input-gradient GEMM); scalesT (nullable, must be given
+ *   together with qT): f32 [K/128][N/128], the same scales transposed.
+ *   Requires N % 128 == 0 and K % 128 == 0.
+ */
+fp8bs_status fp8bs_quant_weight_128x128(const void *w_bf16, int64_t N,
+                                        int64_t K, uint8_t *q, float *scales,
+                                        uint8_t *qT, float *scalesT,
+                                        fp8bs_stream_t stream);
+
+/*
+ * Backward-pass re-tiling [P1¶3]: cached FP8 activations quantized in 1x128
+ * tiles become 128x1 tiles.  Each element is dequantized with one
+ * round-to-nearest FP32 multiply, x_hat = decode(q) * s, and x_hat is
+ * quantized again in groups of 128 consecutive rows of one column, written
+ * transposed.
+ *   q: E4M3 [M][K], scales: f32 [K/128][M]
+ *   -> qT: E4M3 [K][M], scalesT: f32 [M/128][K].
+ *   Requires M % 128 == 0 and K % 128 == 0.
+ */
+fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t *q,
+                                          const float *scales, int64_t M,
+                                          int64_t K, uint8_t *qT,
+                                          float *scalesT,
+                                          fp8bs_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM [P1¶2][P1¶3][P4¶4]: C = A * B^T with
+ *   C[m][n] = sum over K-groups g of sa[g][m] * sB(n, g) * P_g[m][n],
+ *   P_g[m][n] = sum_{k in g} A[m][k] * B[n][k]   (tensor cores, FP8 inputs),
+ * each P_g promoted into an FP32 accumulator on the CUDA cores (one group =
+ * 128 consecutive k).
+ *   a: E4M3 [M][K], sa: f32 [K/128][M]
+ *   b: E4M3 [N][K], sb: f32 [ceil(N/128)][K/128] (BLOCK) or [K/128][N]
+ *   (TILE)
+ *   c: [M][N], bf16 (round-to-nearest-even from FP32) or f32.
+ *   Requires K % 128 == 0, N % 16 == 0, K > 0; M >= 0 (a ragged M tail is
+ *   handled); M == 0 or N == 0 is a no-op.
+ * Returns FP8BS_ERR_TIMEOUT only through fp8bs_get_device_error().
+ */
+fp8bs_status fp8bs_gemm(const uint8_t *a, const float *sa, const uint8_t *b,
+                        const float *sb, fp8bs_bscale_kind bkind, int64_t M,
+                        int64_t N, int64_t K, void *c, fp8bs_out_dtype out,
+                        fp8bs_stream_t stream);
+
+/*
+ * fp8bs_gemm with a choice of accumulation.  promote = 1 is fp8bs_gemm.
+ * promote = 0 is the deliberately un-promoted variant used to measure what
+ * tensor-core-only accumulation costs [P1¶4][P2¶3]: the whole K is
+ * accumulated inside the tensor core and the scales are applied once at
+ * the end, using K-group 0's scales (sa[0][m] and sB(n, 0)).  It is exact
+ * only for operands whose scales are constant along K (row-wise
+ * quantization); it is a measurement tool, not a second product path.
+ */
+fp8bs_status fp8bs_gemm_ex(const uint8_t *a, const float *sa,
+                           const uint8_t *b, const float *sb,
+                           fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                           int64_t K, void *c, fp8bs_out_dtype out,
+                           int promote, fp8bs_stream_t stream);
+
+/* Static English name of a status code. */
+const char *fp8bs_status_string(fp8bs_status status);
+
+/*
+ * Synchronizes `stream`, then reports and clears the device error word that
+ * bounded waits inside the GEMM set when they give up (FP8BS_ERR_TIMEOUT),
+ * or FP8BS_ERR_CUDA if the synchronization itself failed.
+ */
+fp8bs_status fp8bs_get_device_error(fp8bs_stream_t stream);
+
+/* cudaError_t value of the last CUDA failure seen by this host thread
+ * (FP8BS_ERR_CUDA leaves the detail here; 0 if none). */
+int fp8bs_last_cuda_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int fp8bs_version(void);
+
+/*
+ * TEST SUPPORT ONLY -- exercises the GEMM's bounded waits without faulting
+ * or hanging the GPU.  Runs fp8bs_gemm (BLOCK scales, FP32 out, promoted)
+ * except that the TMA producer skips pipeline iteration `skip_iter` (>= 0):
+ * its copy is never issued and its mbarrier never completes, so the
+ * consumer waiting on it gives up after its time limit (about 2 s), every
+ * warp winds down, TMEM is freed and the kernel returns.  The C output is
+ * then undefined; fp8bs_get_device_error() reports FP8BS_ERR_TIMEOUT and
+ * clears the error word, after which the context is usable as before.
+ */
+fp8bs_status fp8bs_debug_gemm_stall(const uint8_t *a, const float *sa,
+                                    const uint8_t *b, const float *sb,
+                                    int64_t M, int64_t N, int64_t K, void *c,
+                                    int skip_iter, fp8bs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every entry point include/fp8bs.h declares, and rejects invalid arguments
+synchronously, before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8bs.h")
+
+
+@pytest.fixture(scope="module")
+def libfp8bs():
+    from fp8_fine_grained_18_b300 import build
+    build.build()
+    import fp8_fine_grained_18_b300 as m
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8bs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("fp8bs_quant_act_1x128", "fp8bs_quant_weight_128x128",
+                     "fp8bs_requant_1x128_to_128x1", "fp8bs_gemm", "fp8bs_gemm_ex",
+                     "fp8bs_status_string", "fp8bs_get_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(libfp8bs):
+    lib = ctypes.CDLL(libfp8bs.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(libfp8bs):
+    lib = libfp8bs.lib()
+    for s in range(7):
+        assert lib.fp8bs_status_string(s)
+    assert lib.fp8bs_status_string(0) == b"ok"
+    assert lib.fp8bs_version() >= 100
+
+
+FAKE = ctypes.c_void_p(0x10000)      # never dereferenced: rejected first
+FAKE_ODD = ctypes.c_void_p(0x10008)  # 8-byte aligned only
+
+
+def test_quant_argument_errors(libfp8bs):
+    L, m = libfp8bs.lib(), libfp8bs
+    # no-ops need no pointers
+    assert L.fp8bs_quant_act_1x128(None, 0, 128, 0, None, None, None) == m.OK
+    assert L.fp8bs_quant_act_1x128(None, 5, 0, 0, None, None, None) == m.OK
+    assert L.fp8bs_quant_act_1x128(FAKE, -1, 128, 0, FAKE, FAKE, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_quant_act_1x128(FAKE, 4, 128, 2, FAKE, FAKE, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_quant_act_1x128(None, 4, 128, 0, FAKE, FAKE, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_quant_act_1x128(FAKE, 4, 100, 0, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_1x128(FAKE, 100, 128, 1, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_1x128(FAKE_ODD, 4, 128, 0, FAKE, FAKE, None) == m.ERR_MISALIGNED
+    assert L.fp8bs_quant_weight_128x128(FAKE, 128, 128, FAKE, FAKE, FAKE, None, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_quant_weight_128x128(FAKE, 100, 128, FAKE, FAKE, None, None, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_weight_128x128(FAKE, 128, 128, FAKE, FAKE_ODD, None, None, None) == m.ERR_MISALIGNED
+    assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 128, 128, FAKE, None, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 129, 128, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+
+
+def test_gemm_argument_errors(libfp8bs):
+    L, m = libfp8bs.lib(), libfp8bs
+    args = lambda M, N, K, bk=0, out=0, pr=1, a=FAKE, c=FAKE: (  # noqa: E731
+        a, FAKE, FAKE, FAKE, bk, M, N, K, c, out, pr, None)
+    assert L.fp8bs_gemm_ex(*args(0, 256, 128)) == m.OK
+    assert L.fp8bs_gemm_ex(*args(8, 0, 128)) == m.OK
+    assert L.fp8bs_gemm_ex(*args(-1, 256, 128)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_ex(*args(8, 256, 128, bk=2)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_ex(*args(8, 256, 128, out=3)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_ex(*args(8, 256, 128, pr=2)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_ex(*args(8, 256, 128, a=None)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_ex(*args(8, 256, 100)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_ex(*args(8, 256, 0)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_ex(*args(8, 250, 128)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_ex(*args(8, 256, 128, c=FAKE_ODD)) == m.ERR_MISALIGNED
+    assert L.fp8bs_debug_gemm_stall(FAKE, FAKE, FAKE, FAKE, 8, 256, 128, FAKE, -1, None) == m.ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_reports_cuda_or_arch(libfp8bs):
+    """On a machine without a usable sm_103 device a valid call must fail
+    with a status, not crash (this is what the CPU suite sees)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    L, m = libfp8bs.lib(), libfp8bs
+    st = L.fp8bs_quant_act_1x128(FAKE, 4, 128, 0, FAKE, FAKE, None)
+    assert st in (m.ERR_CUDA, m.ERR_ARCH)
