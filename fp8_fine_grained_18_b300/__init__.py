@@ -25,7 +25,7 @@ GROUP = 128
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libfp8bs.so is not built ({LIB_PATH}); run "
-                      "`python -m fp8_fine_grained_18_b300.build`")
+                      "`python fp8_fine_grained_18_b300/build.py`")
 
 _lib = ctypes.CDLL(LIB_PATH)
 _P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int

@@ -1,6 +1,6 @@
 """Build libfp8bs.so in-tree for sm_103a with nvcc.
 
-    python -m fp8_fine_grained_18_b300.build [--force] [--verbose]
+    python fp8_fine_grained_18_b300/build.py [--force] [--verbose]
 
 One nvcc invocation per translation unit (objects cached by mtime), then one
 shared-library link.  The CUDA runtime is linked statically; the driver's

@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "fp8bs.h")
 
 @pytest.fixture(scope="module")
 def libfp8bs():
-    from fp8_fine_grained_18_b300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__._load_builder().build()
     import fp8_fine_grained_18_b300 as m
     return m
 
