@@ -73,34 +73,32 @@ class ClockSampler:
                0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
 
     def __init__(self, torch_device):
-        self.samples, self.reasons, self.ok = [], set(), False
+        self.samples, self.reasons, self.ok, self.err = [], set(), False, None
         self._stop = threading.Event()
+        self.max_mhz = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            try:
-                import torch
-                bus = torch.cuda.get_device_properties(torch_device).pci_bus_id
-                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-            except Exception:
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(torch_device)
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(int(torch_device))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self._reasons_fn = fn or pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
             self.ok = True
-        except Exception:
-            self.max_mhz = None
+        except Exception as e:  # noqa: BLE001 -- reported in the JSON line
+            self.err = f"{type(e).__name__}: {e}"
 
     def _run(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM))
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                r = self._reasons_fn(self.h)
                 for bit, name in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:  # noqa: BLE001
+                self.err = f"{type(e).__name__}: {e}"
             time.sleep(0.005)
 
     def __enter__(self):
@@ -115,11 +113,12 @@ class ClockSampler:
             self.t.join()
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                    "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
+               "samples": len(self.samples), "source": "NVML, 5 ms polling"}
+        if self.err:
+            out["error"] = self.err
+        return out
 
 
 # ---------------------------------------------------------------- our arm
@@ -453,7 +452,7 @@ def _ref_step(oracle, inp, qw, sw, r0, rows, N, K):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", type=int, default=1, help="also time every hot-path row (1/0)")

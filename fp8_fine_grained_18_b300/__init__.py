@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
 OUT_BF16, OUT_F32 = 0, 1
+TILE_AUTO, TILE_128x128, TILE_128x224_CLUSTER2, TILE_128x256_CLUSTER2 = -1, 0, 1, 2
 BSCALE_BLOCK_128x128, BSCALE_TILE_1x128 = 0, 1
 GROUP = 128
 
@@ -36,7 +37,8 @@ _SIGS = {
     "fp8bs_requant_1x128_to_128x1": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8bs_gemm": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P],
     "fp8bs_gemm_ex": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _P],
-    "fp8bs_debug_gemm_stall": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I, _P],
+    "fp8bs_gemm_tiled": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _I, _P],
+    "fp8bs_debug_gemm_stall": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I, _I, _P],
     "fp8bs_get_device_error": [_P],
     "fp8bs_status_string": [_I],
     "fp8bs_last_cuda_error": [],
@@ -130,25 +132,29 @@ def requant_1x128_to_128x1(q: torch.Tensor, scales: torch.Tensor, qT=None, scale
 
 def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
          bkind: int = BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, promote: bool = True,
-         out=None):
-    """C[M, N] = block-scaled a[M, K] * b[N, K]^T (bf16 or float32 out)."""
+         out=None, tile: int = TILE_AUTO):
+    """C[M, N] = block-scaled a[M, K] * b[N, K]^T (bf16 or float32 out).
+
+    tile: TILE_AUTO (per-shape choice) or one of the TILE_* shapes."""
     assert a.dtype == torch.uint8 and b.dtype == torch.uint8
     M, K = a.shape
     N = b.shape[0]
     odt = OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32
     c = _empty((M, N), out_dtype, a) if out is None else out
-    _check(_lib.fp8bs_gemm_ex(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K, _ptr(c),
-                              odt, int(bool(promote)), _stream(a)), "fp8bs_gemm")
+    _check(_lib.fp8bs_gemm_tiled(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K,
+                                 _ptr(c), odt, int(bool(promote)), int(tile), _stream(a)),
+           "fp8bs_gemm")
     return c
 
 
-def debug_gemm_stall(a, sa, b, sb, skip_iter: int, out=None):
+def debug_gemm_stall(a, sa, b, sb, skip_iter: int, out=None, tile: int = TILE_AUTO):
     """Test support: see fp8bs_debug_gemm_stall in include/fp8bs.h."""
     M, K = a.shape
     N = b.shape[0]
     c = _empty((M, N), torch.float32, a) if out is None else out
     _check(_lib.fp8bs_debug_gemm_stall(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, _ptr(c),
-                                       int(skip_iter), _stream(a)), "fp8bs_debug_gemm_stall")
+                                       int(skip_iter), int(tile), _stream(a)),
+           "fp8bs_debug_gemm_stall")
     return c
 
 

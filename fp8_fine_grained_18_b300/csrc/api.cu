@@ -49,12 +49,14 @@ constexpr int64_t kMaxDim = (int64_t)1 << 31;  // kernels index rows with int32
 
 fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
-                         fp8bs_out_dtype out, int promote, int skip_iter, fp8bs_stream_t stream) {
+                         fp8bs_out_dtype out, int promote, int skip_iter, int tile,
+                         fp8bs_stream_t stream) {
   if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
   if (bkind != FP8BS_BSCALE_BLOCK_128x128 && bkind != FP8BS_BSCALE_TILE_1x128)
     return FP8BS_ERR_INVALID_ARG;
   if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
   if (promote != 0 && promote != 1) return FP8BS_ERR_INVALID_ARG;
+  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_128x256_CLUSTER2) return FP8BS_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FP8BS_OK;
   if (!a || !sa || !b || !sb || !c) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -76,6 +78,7 @@ fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, co
   g.out_bf16 = out == FP8BS_OUT_BF16;
   g.promote = promote != 0;
   g.skip_iter = skip_iter;
+  g.tile = tile;
   return cuda_status(fp8bs::launch_gemm(g, as_cuda(stream)));
 }
 
@@ -137,21 +140,29 @@ fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t* q, const float* scales,
 fp8bs_status fp8bs_gemm(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                         fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
                         fp8bs_out_dtype out, fp8bs_stream_t stream) {
-  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, 1, -1, stream);
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, 1, -1, FP8BS_TILE_AUTO, stream);
 }
 
 fp8bs_status fp8bs_gemm_ex(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                            fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
                            fp8bs_out_dtype out, int promote, fp8bs_stream_t stream) {
-  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, promote, -1, stream);
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, promote, -1, FP8BS_TILE_AUTO,
+                     stream);
+}
+
+fp8bs_status fp8bs_gemm_tiled(const uint8_t* a, const float* sa, const uint8_t* b,
+                              const float* sb, fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                              int64_t K, void* c, fp8bs_out_dtype out, int promote,
+                              fp8bs_tile_shape tile, fp8bs_stream_t stream) {
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, promote, -1, tile, stream);
 }
 
 fp8bs_status fp8bs_debug_gemm_stall(const uint8_t* a, const float* sa, const uint8_t* b,
                                     const float* sb, int64_t M, int64_t N, int64_t K, void* c,
-                                    int skip_iter, fp8bs_stream_t stream) {
+                                    int skip_iter, fp8bs_tile_shape tile, fp8bs_stream_t stream) {
   if (skip_iter < 0) return FP8BS_ERR_INVALID_ARG;
   return gemm_common(a, sa, b, sb, FP8BS_BSCALE_BLOCK_128x128, M, N, K, c, FP8BS_OUT_F32, 1,
-                     skip_iter, stream);
+                     skip_iter, tile, stream);
 }
 
 const char* fp8bs_status_string(fp8bs_status s) {

@@ -8,16 +8,24 @@
 // paragraph 3; FP8 in, BF16/FP32 out, P4 paragraph 4).
 //
 // B300 design (the pages' H800 WGMMA kernel is prior art only):
-//   * persistent CTAs, one per SM, 128 x BN output tiles;
+//   * persistent CTAs, one per SM, each computing 128 x BN output tiles
+//     (BN = 128, 224 or 256, chosen per shape to limit wave quantization);
+//   * with CM = 2, the two CTAs of a cluster work on vertically adjacent
+//     tiles that share the same B tile: each loads half of it and multicasts
+//     that half into both CTAs' shared memory, which halves the L2->SM
+//     traffic of B;
 //   * warp 0 -- TMA producer: A and B K-group tiles (128 B rows, 128-byte
-//     swizzle) into an STAGES-deep shared-memory ring (mbarrier full/empty);
+//     swizzle) into a STAGES-deep shared-memory ring (mbarrier full/empty;
+//     with CM = 2 a stage is free only once both CTAs' MMAs have read it);
 //   * warp 1 -- MMA issuer: per K-group, four tcgen05.mma kind::f8f6f4
-//     (K = 32 each) into one of TBUF TMEM partial buffers, then
+//     (K = 32 each) into one of the TMEM partial buffers, then
 //     tcgen05.commit to free the smem stage and to publish the partial;
 //   * warp 2 -- scale loader: the K-group's 128 row scales of A and the
-//     tile's B scales into a small shared ring;
+//     tile's B scales into a small shared ring, by cp.async completing on an
+//     mbarrier, so it never waits for memory itself;
 //   * warps 4..11 -- promotion: each owns 32 TMEM lanes (rows) and half the
-//     tile's columns, keeps the FP32 accumulator in registers, and per
+//     tile's columns, keeps the FP32 accumulator in registers (setmaxnreg
+//     moves registers from warps 0-3 to these when BN > 128), and per
 //     K-group does acc += P_g * (sa * sb) while the tensor core already
 //     computes the next group's partial into the other TMEM buffer (the
 //     "overlapping of the two operations" of P3 paragraph 4 / P4 paragraph 1);
@@ -48,7 +56,14 @@ constexpr int kThreads = 384;       // 12 warps
 constexpr int kFirstPromoWarp = 4;  // warps 4..11
 constexpr int kPromoWarps = 8;
 constexpr int kScaleSlots = 8;
+constexpr int kSmemLimit = 232448;  // 227 KB: the opt-in maximum per block
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
+// Register split when the accumulators need more than an even share:
+// warpgroup 0 (producer, MMA, scales) keeps kCtlRegs, the two promotion
+// warpgroups get kPromoRegs.  Their sum must fit in what the launch holds.
+constexpr int kCtlRegs = 40;
+constexpr int kPromoRegs = 232;
+constexpr int kSplitRegsNeeded = 128 * kCtlRegs + 256 * kPromoRegs;
 
 enum : unsigned int {
   kErrProducer = 1u,
@@ -63,7 +78,7 @@ struct Params {
   const float* sb;
   void* c;
   int M, N, K, KB;
-  int num_m_tiles, num_tiles;
+  int num_m_units, num_units;  // a unit = CM vertically adjacent 128 x BN tiles
   int skip_iter;
 };
 
@@ -87,39 +102,65 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-template <int BN, int STAGES, int TBUF>
-struct Smem {
-  static constexpr int kABytes = kBM * kBK;          // 16 KB
+template <int BN, int CM>
+struct Cfg {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(CM == 1 || CM == 2, "CM");
+  static constexpr int kBH = BN / CM;  // B rows this CTA loads (multicast when CM = 2)
+  static_assert(kBH % 8 == 0, "B half must be whole 8-row swizzle atoms");
+  static constexpr int kTmemStride = BN <= 128 ? 128 : 256;  // columns between partials
+  static constexpr int kTBuf = 512 / kTmemStride;            // 4 or 2 partial buffers
+  static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
-  static constexpr int kScaleB = BN + 4;             // B scales per slot
+  static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
   static constexpr int kScaleFloats = kBM + kScaleB;
+  static constexpr int kNumBarsMax = 2 * 8 + 2 * 4 + 2 * kScaleSlots + 1;
+  static constexpr int kFixed = kScaleSlots * kScaleFloats * 4 + kNumBarsMax * 8 + 16 + 1024;
+  static constexpr int kStagesFit = (kSmemLimit - kFixed) / (kABytes + kBBytes);
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static_assert(kStages >= 2, "shared memory");
   static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + STAGES * kABytes;
-  static constexpr int kOffScale = kOffB + STAGES * kBBytes;
+  static constexpr int kOffB = kOffA + kStages * kABytes;
+  static constexpr int kOffScale = kOffB + kStages * kBBytes;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleFloats * 4;
-  static constexpr int kNumBars = 2 * STAGES + 2 * TBUF + 2 * kScaleSlots + 1;
+  static constexpr int kNumBars = 2 * kStages + 2 * kTBuf + 2 * kScaleSlots + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+  static_assert(kAlloc <= kSmemLimit, "shared memory");
+  static constexpr bool kRegSplit = BN > 128;
 };
 
-__host__ __device__ constexpr int tmem_cols_for(int cols) {
-  return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-template <int BN, int STAGES, int TBUF, bool PROMOTE, bool OUT_BF16, bool B_TILE>
+// Load step `st` (columns [32 st, 32 st + 32) of a warp's kHalf columns, or
+// the last 16 when kHalf is not a multiple of 32) from TMEM into r.
+template <int kHalf>
+__device__ __forceinline__ void tmem_ld_step(uint32_t taddr, int st, uint32_t* r) {
+  ptx::tmem_ld_32x32b_x16(taddr + st * 32, r);
+  if (st * 32 + 16 < kHalf) ptx::tmem_ld_32x32b_x16(taddr + st * 32 + 16, r + 16);
+}
+
+template <int BN, int CM, bool PROMOTE, bool OUT_BF16, bool B_TILE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  using L = Smem<BN, STAGES, TBUF>;
-  static_assert(BN % 64 == 0 && BN <= 256, "BN");
-  static_assert(BN * TBUF <= 512, "TMEM");
-  constexpr int kHalf = BN / 2;        // columns per promotion warp
-  constexpr int kChunks = kHalf / 32;  // 32-column TMEM loads per warp
-  constexpr int kChunksPerRound = kChunks < 2 ? kChunks : 2;
-  constexpr uint32_t kTmemCols = tmem_cols_for(BN * TBUF);
+  using L = Cfg<BN, CM>;
+  constexpr int STAGES = L::kStages;
+  constexpr int TBUF = L::kTBuf;
+  constexpr int kHalf = BN / 2;         // columns per promotion warp
+  constexpr int kSteps = (kHalf + 31) / 32;  // 32-column TMEM load steps per K-group
+  // step 0 of every K-group uses staging buffer 0, so the last step of the
+  // previous K-group must use buffer 1
+  static_assert(kSteps % 2 == 0, "even number of TMEM load steps");
+  constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kBM, BN);
-  constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;
+  constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;  // bytes landing in this CTA
+  constexpr uint16_t kPeers = (1u << CM) - 1u;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -140,11 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = CM > 1 ? (int)ptx::cluster_ctarank() : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&empty[i], 1);
+      ptx::mbar_init(&empty[i], CM);  // one MMA commit from each CTA of the cluster
     }
     for (int i = 0; i < TBUF; ++i) {
       ptx::mbar_init(&tfull[i], 1);
@@ -165,10 +207,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // the peer's barriers must be initialised before any multicast reaches them
+  if (CM > 1) ptx::cluster_sync();
   const uint32_t tmem_base = *tmem_base_slot;
 
   const int KB = p.KB;
+  const int unit_first = blockIdx.x / CM;
+  const int unit_stride = gridDim.x / CM;
 
+  if (warp < kFirstPromoWarp) {
+  // Warpgroup 0: producer, MMA issuer, scale loader (warp 3 idles).  Each
+  // warpgroup changes its register allocation at the top of its own branch,
+  // so that the code it runs is compiled against the new limit.
+  if constexpr (L::kRegSplit) ptx::regs_dec<kCtlRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -177,15 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       uint32_t issued_mask = 0;  // stages with a copy issued at least once
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+        const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
           if (!wait_bar(&empty[stage], phase ^ 1, abort_flag, kErrProducer)) { ok = false; break; }
           if ((int)it == p.skip_iter) continue;  // test hook: never arrives
           ptx::mbar_arrive_expect_tx(&full[stage], kStageTx);
           ptx::tma_load_2d(sA + stage * L::kABytes, &tmap_a, &full[stage], kb * kBK, mt * kBM);
-          ptx::tma_load_2d(sB + stage * L::kBBytes, &tmap_b, &full[stage], kb * kBK, nt * BN);
+          if (CM == 1)
+            ptx::tma_load_2d(sB + stage * L::kBBytes, &tmap_b, &full[stage], kb * kBK, nt * BN);
+          else
+            ptx::tma_load_2d_mcast(sB + stage * L::kBBytes + rank * L::kBH * kBK, &tmap_b,
+                                   &full[stage], kb * kBK, nt * BN + rank * L::kBH, kPeers);
           issued_mask |= 1u << stage;
         }
       }
@@ -209,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, kt = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
         if (PROMOTE) {
           for (int kb = 0; kb < KB; ++kb, ++it, ++kt) {
             const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
@@ -220,19 +275,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
-            const uint32_t d = tmem_base + buf * BN;
+            const uint32_t d = tmem_base + buf * L::kTmemStride;
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k)
               ptx::mma_f8f6f4(d, ptx::smem_desc_k128_sw128(a0 + 32 * k),
                               ptx::smem_desc_k128_sw128(b0 + 32 * k), kIdesc, k > 0);
-            ptx::tc_commit(&empty[stage]);
+            if (CM == 1)
+              ptx::tc_commit(&empty[stage]);
+            else
+              ptx::tc_commit_mcast(&empty[stage], kPeers);
             ptx::tc_commit(&tfull[buf]);
           }
         } else {
           const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
           if (!wait_bar(&tempty[buf], tph ^ 1, abort_flag, kErrMma)) break;
           ptx::tc_fence_after();
-          const uint32_t d = tmem_base + buf * BN;
+          const uint32_t d = tmem_base + buf * L::kTmemStride;
           for (int kb = 0; kb < KB; ++kb, ++it) {
             const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
             if (!wait_bar(&full[stage], phase, abort_flag, kErrMma)) { ok = false; break; }
@@ -244,7 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::mma_f8f6f4(d, ptx::smem_desc_k128_sw128(a0 + 32 * k),
                               ptx::smem_desc_k128_sw128(b0 + 32 * k), kIdesc,
                               (kb > 0 || k > 0) ? 1u : 0u);
-            ptx::tc_commit(&empty[stage]);
+            if (CM == 1)
+              ptx::tc_commit(&empty[stage]);
+            else
+              ptx::tc_commit_mcast(&empty[stage], kPeers);
           }
           if (!ok) break;
           ptx::tc_commit(&tfull[buf]);
@@ -264,37 +325,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PROMOTE) {
       uint32_t ks = 0;
       bool ok = true;
-      const int nb_first_stride = p.KB;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+      for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+        const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
         const int m0 = mt * kBM, n0 = nt * BN;
+        const int nb_first = n0 / 128;
+        const int nb_count = (n0 + BN - 1) / 128 - nb_first + 1;
         for (int kb = 0; kb < KB; ++kb, ++ks) {
           const uint32_t slot = ks % kScaleSlots, sph = (ks / kScaleSlots) & 1;
           bool w = wait_bar(&sempty[slot], sph ^ 1, abort_flag, kErrScales);
           if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+          // Asynchronous 4-byte copies (zero-filled outside the matrix) that
+          // complete on sfull[slot]: the loader never waits for memory, so it
+          // runs up to kScaleSlots K-groups ahead of the promotion warps.
           float* dst = sScale + slot * L::kScaleFloats;
 #pragma unroll
           for (int i = 0; i < kBM / 32; ++i) {
             const int r = lane + 32 * i, m = m0 + r;
-            dst[r] = (m < p.M) ? __ldg(p.sa + (size_t)kb * p.M + m) : 0.0f;
+            const bool v = m < p.M;
+            ptx::cp_async_4(dst + r, v ? p.sa + (size_t)kb * p.M + m : p.sa, v);
           }
           float* dstb = dst + kBM;
           if (B_TILE) {
 #pragma unroll
             for (int i = 0; i < BN / 32; ++i) {
               const int cidx = lane + 32 * i, n = n0 + cidx;
-              dstb[cidx] = (n < p.N) ? __ldg(p.sb + (size_t)kb * p.N + n) : 0.0f;
+              const bool v = n < p.N;
+              ptx::cp_async_4(dstb + cidx, v ? p.sb + (size_t)kb * p.N + n : p.sb, v);
             }
-          } else if (lane < 4) {
-            const int nb = n0 / 128 + lane;
-            dstb[lane] = (nb * 128 < p.N) ? __ldg(p.sb + (size_t)nb * nb_first_stride + kb) : 0.0f;
+          } else if (lane < nb_count) {
+            const int nb = nb_first + lane;
+            const bool v = nb * 128 < p.N;
+            ptx::cp_async_4(dstb + lane, v ? p.sb + (size_t)nb * KB + kb : p.sb, v);
           }
-          ptx::mbar_arrive(&sfull[slot]);
+          ptx::cp_async_arrive_noinc(&sfull[slot]);
         }
       }
+      // no copy may still be in flight into shared memory when the CTA exits
+      ptx::cp_async_wait_all();
     }
-  } else if (warp >= kFirstPromoWarp) {
+  }
+  } else {
     // ------------------------------------------------- promotion + epilogue
+    if constexpr (L::kRegSplit) ptx::regs_inc<kPromoRegs>();
     const int w = warp - kFirstPromoWarp;
     const int lg = warp & 3;       // TMEM lane group this warp may access
     const int ch = w >> 2;         // column half
@@ -303,63 +375,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = (uint32_t)(lg * 32) << 16;
     uint32_t kt = 0, ks = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const int mt = tile % p.num_m_tiles, nt = tile / p.num_m_tiles;
+    for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+      const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
       const int m0 = mt * kBM, n0 = nt * BN;
       float acc[kHalf];
 #pragma unroll
       for (int j = 0; j < kHalf; ++j) acc[j] = 0.0f;
 
       if (PROMOTE) {
+        // Software pipeline over 32-column steps (kSteps per K-group): the
+        // TMEM load of step s+1 is issued right after step s's data has
+        // arrived and before step s's FMAs, so its latency hides behind
+        // them.  tcgen05.wait::ld waits for all of this thread's loads, which
+        // is why only one step is ever in flight.
+        uint32_t v[2][32];
+        uint32_t buf = kt % TBUF;
+        {
+          const uint32_t tph = (kt / TBUF) & 1;
+          bool w0 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
+          if (!__all_sync(0xFFFFFFFFu, w0)) { ok = false; break; }
+          ptx::tc_fence_after();
+          tmem_ld_step<kHalf>(tmem_base + t_lane + buf * L::kTmemStride + col0, 0, v[0]);
+        }
         for (int kb = 0; kb < KB; ++kb, ++kt, ++ks) {
-          const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
           const uint32_t slot = ks % kScaleSlots, sph = (ks / kScaleSlots) & 1;
           bool w1 = wait_bar(&sfull[slot], sph, abort_flag, kErrPromo);
-          bool w2 = w1 && wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
-          if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
-          ptx::tc_fence_after();
+          if (!__all_sync(0xFFFFFFFFu, w1)) { ok = false; break; }
           const float* sc = sScale + slot * L::kScaleFloats;
           const float sa_r = sc[row];
           const float* scb = sc + kBM;
-          const uint32_t tbase = tmem_base + t_lane + buf * BN + col0;
+          const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
 #pragma unroll
-          for (int c0 = 0; c0 < kChunks; c0 += kChunksPerRound) {
-            uint32_t v[kChunksPerRound][32];
-#pragma unroll
-            for (int cc = 0; cc < kChunksPerRound; ++cc)
-              ptx::tmem_ld_32x32b_x32(tbase + (c0 + cc) * 32, v[cc]);
+          for (int st = 0; st < kSteps; ++st) {
             ptx::tmem_ld_wait();
-#pragma unroll
-            for (int cc = 0; cc < kChunksPerRound; ++cc) ptx::reg_barrier(v[cc]);
-            if (c0 + kChunksPerRound >= kChunks) {
-              // every TMEM read of this buffer is done: hand it back
+            reg_fence<32>(v[st & 1]);
+            if (st + 1 < kSteps) {
+              tmem_ld_step<kHalf>(tcur, st + 1, v[(st + 1) & 1]);
+            } else {
+              // every TMEM read of this buffer is done: hand it back, then
+              // start on the next K-group's partial
               ptx::tc_fence_before();
               __syncwarp();
               if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+              if (kb + 1 < KB) {
+                const uint32_t kn = kt + 1;
+                buf = kn % TBUF;
+                bool w2 = wait_bar(&tfull[buf], (kn / TBUF) & 1, abort_flag, kErrPromo);
+                if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
+                ptx::tc_fence_after();
+                tmem_ld_step<kHalf>(tmem_base + t_lane + buf * L::kTmemStride + col0, 0,
+                                    v[0]);
+              }
             }
+            const uint32_t* cur = v[st & 1];
 #pragma unroll
-            for (int cc = 0; cc < kChunksPerRound; ++cc) {
-              const int cbase = col0 + (c0 + cc) * 32;
+            for (int h = 0; h < 2; ++h) {
+              const int a0 = st * 32 + h * 16;  // accumulator index of this 16-column part
+              if (a0 >= kHalf) break;
+              const int cbase = col0 + a0;
               if (B_TILE) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < 16; ++j) {
                   const float f = __fmul_rn(sa_r, scb[cbase + j]);
-                  acc[(c0 + cc) * 32 + j] =
-                      __fmaf_rn(__uint_as_float(v[cc][j]), f, acc[(c0 + cc) * 32 + j]);
+                  acc[a0 + j] = __fmaf_rn(__uint_as_float(cur[h * 16 + j]), f, acc[a0 + j]);
                 }
               } else {
                 const int nbi = (n0 + cbase) / 128 - n0 / 128;
                 const float f = __fmul_rn(sa_r, scb[nbi]);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  acc[(c0 + cc) * 32 + j] =
-                      __fmaf_rn(__uint_as_float(v[cc][j]), f, acc[(c0 + cc) * 32 + j]);
+                for (int j = 0; j < 16; ++j)
+                  acc[a0 + j] = __fmaf_rn(__uint_as_float(cur[h * 16 + j]), f, acc[a0 + j]);
               }
             }
           }
+          if (!ok) break;
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sempty[slot]);
         }
+        if (!ok) break;
       } else {
         const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
         bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
@@ -367,26 +460,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int m = m0 + row;
         const float sa_r = (m < p.M) ? __ldg(p.sa + m) : 0.0f;  // K-group 0
-        const uint32_t tbase = tmem_base + t_lane + buf * BN + col0;
+        const uint32_t tbase = tmem_base + t_lane + buf * L::kTmemStride + col0;
 #pragma unroll
-        for (int c0 = 0; c0 < kChunks; c0 += kChunksPerRound) {
-          uint32_t v[kChunksPerRound][32];
-#pragma unroll
-          for (int cc = 0; cc < kChunksPerRound; ++cc)
-            ptx::tmem_ld_32x32b_x32(tbase + (c0 + cc) * 32, v[cc]);
+        for (int c0 = 0; c0 < kHalf / 16; ++c0) {
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(tbase + c0 * 16, v);
           ptx::tmem_ld_wait();
+          reg_fence<16>(v);
 #pragma unroll
-          for (int cc = 0; cc < kChunksPerRound; ++cc) ptx::reg_barrier(v[cc]);
-#pragma unroll
-          for (int cc = 0; cc < kChunksPerRound; ++cc) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int n = n0 + col0 + (c0 + cc) * 32 + j;
-              float sbv = 0.0f;
-              if (n < p.N) sbv = B_TILE ? __ldg(p.sb + n) : __ldg(p.sb + (size_t)(n / 128) * p.KB);
-              acc[(c0 + cc) * 32 + j] =
-                  __fmul_rn(__uint_as_float(v[cc][j]), __fmul_rn(sa_r, sbv));
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int n = n0 + col0 + c0 * 16 + j;
+            float sbv = 0.0f;
+            if (n < p.N) sbv = B_TILE ? __ldg(p.sb + n) : __ldg(p.sb + (size_t)(n / 128) * p.KB);
+            acc[c0 * 16 + j] = __fmul_rn(__uint_as_float(v[j]), __fmul_rn(sa_r, sbv));
           }
         }
         ptx::tc_fence_before();
@@ -438,6 +524,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (CM > 1) {
+    // After an abort a peer's multicast may still be landing in this CTA's
+    // shared memory: give it time before leaving (normal runs skip this).
+    if (*abort_flag) {
+      const uint64_t t0 = ptx::globaltimer();
+      while (ptx::globaltimer() - t0 < 1000000ull) {
+      }
+    }
+    // neither CTA leaves while the other may still write into it
+    ptx::cluster_sync();
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -477,6 +574,8 @@ bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, i
   return r == CUDA_SUCCESS;
 }
 
+constexpr int kMaxDevices = 64;
+
 int num_sms_current_device() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -484,14 +583,62 @@ int num_sms_current_device() {
   return n > 0 ? n : 1;
 }
 
-template <int BN, int STAGES, int TBUF, bool PROMOTE, bool OUT_BF16, bool B_TILE>
+// Per-device, per-kernel launch facts, computed on first use: the
+// shared-memory attribute is set, the register split is checked against
+// what the compiled kernel is launched with, and for clusters the number of
+// clusters that fit on the device at once.
+struct KernelInfo {
+  bool ready = false;
+  cudaError_t err = cudaSuccess;
+  int max_ctas = 0;  // persistent grid size (a multiple of CM)
+};
+
+template <int BN, int CM, bool PROMOTE, bool OUT_BF16, bool B_TILE>
 cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
-  using L = Smem<BN, STAGES, TBUF>;
-  auto kern = gemm_kernel<BN, STAGES, TBUF, PROMOTE, OUT_BF16, B_TILE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  using L = Cfg<BN, CM>;
+  auto kern = gemm_kernel<BN, CM, PROMOTE, OUT_BF16, B_TILE>;
+  static KernelInfo info[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  KernelInfo& ki = info[dev];
+  if (!ki.ready) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e == cudaSuccess && L::kRegSplit) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      // setmaxnreg.inc waits until the registers it asks for are free: a
+      // split larger than the launch's allocation would never proceed.
+      if (e == cudaSuccess && fa.numRegs * kThreads < kSplitRegsNeeded)
+        e = cudaErrorInvalidConfiguration;
+    }
+    int ctas = num_sms_current_device();
+    if (e == cudaSuccess && CM > 1) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(CM * 64);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = L::kAlloc;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CM;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e == cudaSuccess && clusters < 1) e = cudaErrorInvalidConfiguration;
+      ctas = clusters * CM;
+    }
+    ki.err = e;
+    ki.max_ctas = ctas;
+    ki.ready = true;
+  }
+  if (ki.err != cudaSuccess) return ki.err;
+
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, g.a, g.M, g.K, kBM) || !make_tmap(&tb, g.b, g.N, g.K, BN))
+  if (!make_tmap(&ta, g.a, g.M, g.K, kBM) || !make_tmap(&tb, g.b, g.N, g.K, L::kBH))
     return cudaErrorInvalidValue;
   Params p;
   p.sa = g.sa;
@@ -501,25 +648,79 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   p.N = (int)g.N;
   p.K = (int)g.K;
   p.KB = (int)(g.K / kBK);
-  p.num_m_tiles = (int)((g.M + kBM - 1) / kBM);
-  const int num_n_tiles = (int)((g.N + BN - 1) / BN);
-  p.num_tiles = p.num_m_tiles * num_n_tiles;
+  const int m_tiles = (int)((g.M + kBM - 1) / kBM);
+  p.num_m_units = (m_tiles + CM - 1) / CM;
+  const int n_tiles = (int)((g.N + BN - 1) / BN);
+  p.num_units = p.num_m_units * n_tiles;
   p.skip_iter = g.skip_iter;
-  int grid = num_sms_current_device();
-  if (grid > p.num_tiles) grid = p.num_tiles;
-  kern<<<grid, kThreads, L::kAlloc, stream>>>(ta, tb, p);
+  int units = ki.max_ctas / CM;
+  if (units > p.num_units) units = p.num_units;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(units * CM);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CM > 1 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
+// Tile shape per problem.  Each candidate's cost is the number of waves it
+// needs times its tile width over a relative efficiency (wider tiles and
+// clusters that share B tiles move fewer bytes per flop); the cheapest wins.
+enum TileShape { kTile128x128 = 0, kTile128x224x2 = 1, kTile128x256x2 = 2 };
+
+TileShape choose_tile(int64_t M, int64_t N, int sms) {
+  struct Cand {
+    TileShape s;
+    int bn, cm;
+    double eff;
+  };
+  const Cand cands[] = {{kTile128x256x2, 256, 2, 1.0},
+                        {kTile128x224x2, 224, 2, 1.0},
+                        {kTile128x128, 128, 1, 0.7}};
+  TileShape best = kTile128x128;
+  double best_cost = 1e300;
+  const int64_t m_tiles = (M + kBM - 1) / kBM;
+  for (const Cand& c : cands) {
+    const int64_t units = ((m_tiles + c.cm - 1) / c.cm) * ((N + c.bn - 1) / c.bn);
+    const int64_t slots = sms / c.cm;
+    const int64_t waves = (units + slots - 1) / slots;
+    const double cost = (double)waves * c.bn / c.eff;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c.s;
+    }
+  }
+  return best;
+}
+
 template <bool PROMOTE, bool OUT_BF16, bool B_TILE>
-cudaError_t launch_bn(const GemmArgs& g, cudaStream_t stream) {
-  return launch_variant<128, 6, 4, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
+  int shape = g.tile;
+  if (shape < 0) shape = choose_tile(g.M, g.N, num_sms_current_device());
+  switch (shape) {
+    case kTile128x256x2:
+      return launch_variant<256, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile128x224x2:
+      return launch_variant<224, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    default:
+      return launch_variant<128, 1, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+  }
 }
 
 template <bool PROMOTE, bool OUT_BF16>
 cudaError_t launch_bt(const GemmArgs& g, cudaStream_t stream) {
-  return g.b_tile ? launch_bn<PROMOTE, OUT_BF16, true>(g, stream)
-                  : launch_bn<PROMOTE, OUT_BF16, false>(g, stream);
+  return g.b_tile ? launch_shape<PROMOTE, OUT_BF16, true>(g, stream)
+                  : launch_shape<PROMOTE, OUT_BF16, false>(g, stream);
 }
 
 template <bool PROMOTE>

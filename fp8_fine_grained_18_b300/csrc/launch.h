@@ -27,6 +27,7 @@ struct GemmArgs {
   bool out_bf16;
   bool promote;
   int skip_iter;  // test hook: producer skips this pipeline iteration (-1: never)
+  int tile;       // fp8bs_tile_shape value; -1 chooses per problem shape
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);

@@ -153,6 +153,34 @@ fp8bs_status fp8bs_gemm_ex(const uint8_t *a, const float *sa,
                            int64_t K, void *c, fp8bs_out_dtype out,
                            int promote, fp8bs_stream_t stream);
 
+/*
+ * Output tile shapes of the GEMM.  Every shape computes the same result;
+ * they differ in speed.  FP8BS_TILE_AUTO (what fp8bs_gemm uses) picks, per
+ * problem, the shape that needs the fewest full waves of tiles over the
+ * device's SMs, weighted by each shape's efficiency.
+ *   128x128            one CTA per tile;
+ *   128x224, 128x256   clusters of two CTAs on vertically adjacent tiles
+ *                      that share (and multicast) the B tile.
+ */
+typedef enum {
+  FP8BS_TILE_AUTO = -1,
+  FP8BS_TILE_128x128 = 0,
+  FP8BS_TILE_128x224_CLUSTER2 = 1,
+  FP8BS_TILE_128x256_CLUSTER2 = 2
+} fp8bs_tile_shape;
+
+/*
+ * fp8bs_gemm_ex with an explicit tile shape (tuning and testing; every
+ * shape must give results within the same tolerance).  An out-of-range
+ * `tile` returns FP8BS_ERR_INVALID_ARG.
+ */
+fp8bs_status fp8bs_gemm_tiled(const uint8_t *a, const float *sa,
+                              const uint8_t *b, const float *sb,
+                              fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                              int64_t K, void *c, fp8bs_out_dtype out,
+                              int promote, fp8bs_tile_shape tile,
+                              fp8bs_stream_t stream);
+
 /* Static English name of a status code. */
 const char *fp8bs_status_string(fp8bs_status status);
 
@@ -172,18 +200,20 @@ int fp8bs_version(void);
 
 /*
  * TEST SUPPORT ONLY -- exercises the GEMM's bounded waits without faulting
- * or hanging the GPU.  Runs fp8bs_gemm (BLOCK scales, FP32 out, promoted)
- * except that the TMA producer skips pipeline iteration `skip_iter` (>= 0):
- * its copy is never issued and its mbarrier never completes, so the
- * consumer waiting on it gives up after its time limit (about 2 s), every
- * warp winds down, TMEM is freed and the kernel returns.  The C output is
- * then undefined; fp8bs_get_device_error() reports FP8BS_ERR_TIMEOUT and
- * clears the error word, after which the context is usable as before.
+ * or hanging the GPU.  Runs fp8bs_gemm_tiled (BLOCK scales, FP32 out,
+ * promoted, the given tile shape) except that the TMA producer skips
+ * pipeline iteration `skip_iter` (>= 0): its copy is never issued and its
+ * mbarrier never completes, so the consumer waiting on it gives up after its
+ * time limit (about 2 s), every warp winds down, TMEM is freed and the
+ * kernel returns.  The C output is then undefined; fp8bs_get_device_error()
+ * reports FP8BS_ERR_TIMEOUT and clears the error word, after which the
+ * context is usable as before.
  */
 fp8bs_status fp8bs_debug_gemm_stall(const uint8_t *a, const float *sa,
                                     const uint8_t *b, const float *sb,
                                     int64_t M, int64_t N, int64_t K, void *c,
-                                    int skip_iter, fp8bs_stream_t stream);
+                                    int skip_iter, fp8bs_tile_shape tile,
+                                    fp8bs_stream_t stream);
 
 #ifdef __cplusplus
 }

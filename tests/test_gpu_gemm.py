@@ -13,6 +13,8 @@ from tests._helpers import (assert_gemm_bf16, assert_gemm_f32, dev, dev_bf16, ge
 pytestmark = pytest.mark.gpu
 
 BLOCK, TILE = 0, 1
+# every output-tile shape of the kernel (the automatic choice differs by shape)
+TILES = [0, 1, 2]
 
 
 def _quantized_pair(oracle_mod, M, N, K, seed, bkind):
@@ -44,20 +46,24 @@ def test_tiny(fp8bs, oracle_mod, bkind, out):
         assert_gemm_bf16(c, ref, "tiny")
 
 
+@pytest.mark.parametrize("tile", TILES)
 @pytest.mark.parametrize("M,N,K,bkind", [
     (1, 128, 128, BLOCK), (100, 256, 256, BLOCK), (129, 384, 512, BLOCK), (333, 128, 1024, BLOCK),
     (256, 640, 384, BLOCK), (200, 256, 256, TILE), (385, 512, 640, TILE), (128, 1024, 128, BLOCK),
-    (64, 144, 256, TILE), (130, 208, 384, TILE)])
-def test_ragged_shapes(fp8bs, oracle_mod, M, N, K, bkind):
+    (64, 144, 256, TILE), (130, 208, 384, TILE), (640, 912, 256, BLOCK), (520, 464, 384, TILE)])
+def test_ragged_shapes(fp8bs, oracle_mod, M, N, K, bkind, tile):
     a, sa, b, sb = _quantized_pair(oracle_mod, M, N, K, M + N + K, bkind)
     ref = oracle_mod.gemm(a, sa, b, sb, bkind)
-    c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), bkind, out_dtype=torch.float32))
-    assert_gemm_f32(c, ref, f"{M}x{N}x{K}")
-    c16 = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), bkind, out_dtype=torch.bfloat16))
-    assert_gemm_bf16(c16, ref, f"{M}x{N}x{K} bf16")
+    c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), bkind, out_dtype=torch.float32,
+                        tile=tile))
+    assert_gemm_f32(c, ref, f"{M}x{N}x{K} tile {tile}")
+    c16 = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), bkind, out_dtype=torch.bfloat16,
+                          tile=tile))
+    assert_gemm_bf16(c16, ref, f"{M}x{N}x{K} bf16 tile {tile}")
 
 
-def test_integer_case_bit_exact(fp8bs, oracle_mod):
+@pytest.mark.parametrize("tile", TILES)
+def test_integer_case_bit_exact(fp8bs, oracle_mod, tile):
     """Unit scales and small-integer codes: every partial and the FP32
     accumulator are exact, so the output must equal the integer matmul."""
     rng = np.random.default_rng(21)
@@ -73,11 +79,13 @@ def test_integer_case_bit_exact(fp8bs, oracle_mod):
     b = np.vectorize(vals.get)(bi).astype(np.uint8)
     sa = np.ones((K // 128, M), np.float32)
     sb = np.ones((N // 128, K // 128), np.float32)
-    c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), BLOCK, out_dtype=torch.float32))
+    c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), BLOCK, out_dtype=torch.float32,
+                        tile=tile))
     assert np.array_equal(c.astype(np.int64), ai.astype(np.int64) @ bi.astype(np.int64).T)
 
 
-def test_scale_index_one_hot(fp8bs, oracle_mod):
+@pytest.mark.parametrize("tile", TILES)
+def test_scale_index_one_hot(fp8bs, oracle_mod, tile):
     """Distinct power-of-two scales per (K-group, row) and per B block: a
     misplaced scale index changes the exact result."""
     M, N, K = 256, 384, 512
@@ -94,11 +102,13 @@ def test_scale_index_one_hot(fp8bs, oracle_mod):
     for bkind in (BLOCK, TILE):
         sb = (2.0 ** rng.integers(-5, 6, (N // 128, KB) if bkind == BLOCK else (KB, N))).astype(np.float32)
         ref = oracle_mod.gemm(a, sa, b, sb, bkind)
-        c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), bkind, out_dtype=torch.float32))
-        assert np.array_equal(c.astype(np.float64), ref), bkind
+        c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), bkind, out_dtype=torch.float32,
+                            tile=tile))
+        assert np.array_equal(c.astype(np.float64), ref), (bkind, tile)
 
 
-def test_unpromoted_matches_on_rowwise_codes(fp8bs, oracle_mod):
+@pytest.mark.parametrize("tile", TILES)
+def test_unpromoted_matches_on_rowwise_codes(fp8bs, oracle_mod, tile):
     """The un-promoted variant needs scales constant along K (row-wise
     codes); on such inputs it computes the same sum, with whatever precision
     the tensor core accumulates in.  Its error is measured, not assumed."""
@@ -108,8 +118,9 @@ def test_unpromoted_matches_on_rowwise_codes(fp8bs, oracle_mod):
     b, sb_rows = oracle_mod.quant_rowwise(synth.normal(rng, (N, K), 0.02))
     ref = oracle_mod.gemm(a, sa, b, sb_rows, TILE)
     c_un = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb_rows), TILE, out_dtype=torch.float32,
-                           promote=False))
-    c_pr = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb_rows), TILE, out_dtype=torch.float32))
+                           promote=False, tile=tile))
+    c_pr = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb_rows), TILE, out_dtype=torch.float32,
+                           tile=tile))
     e_un = gemm_errors(c_un, ref)
     e_pr = gemm_errors(c_pr, ref)
     print(f"K={K}: promoted rel_fro={e_pr[0]:.3e} max_rel={e_pr[1]:.3e}; "
@@ -131,17 +142,20 @@ def test_chain_gpu_quant_then_gemm(fp8bs, oracle_mod):
     assert_gemm_f32(c, oracle_mod.gemm(ra, rsa, rb, rsb, BLOCK), "chain")
 
 
-def test_bounded_wait_reports_timeout(fp8bs, oracle_mod):
+@pytest.mark.parametrize("tile", TILES)
+@pytest.mark.parametrize("M,N", [(128, 128), (256, 512)])
+def test_bounded_wait_reports_timeout(fp8bs, oracle_mod, M, N, tile):
     """A pipeline stage whose copy is never issued: the kernel's bounded
     wait expires, the kernel returns, the status reads TIMEOUT, and the
     context keeps working."""
-    a, sa, b, sb = _quantized_pair(oracle_mod, 128, 128, 512, 5, BLOCK)
+    a, sa, b, sb = _quantized_pair(oracle_mod, M, N, 512, 5, BLOCK)
     assert fp8bs.get_device_error() == fp8bs.OK
-    fp8bs.debug_gemm_stall(dev(a), dev(sa), dev(b), dev(sb), skip_iter=2)
+    fp8bs.debug_gemm_stall(dev(a), dev(sa), dev(b), dev(sb), skip_iter=2, tile=tile)
     assert fp8bs.get_device_error() == fp8bs.ERR_TIMEOUT
     assert fp8bs.get_device_error() == fp8bs.OK  # cleared
     ref = oracle_mod.gemm(a, sa, b, sb, BLOCK)
-    c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), BLOCK, out_dtype=torch.float32))
+    c = host(fp8bs.gemm(dev(a), dev(sa), dev(b), dev(sb), BLOCK, out_dtype=torch.float32,
+                        tile=tile))
     assert_gemm_f32(c, ref, "after timeout")
 
 
