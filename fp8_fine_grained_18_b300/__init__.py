@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
 OUT_BF16, OUT_F32 = 0, 1
 TILE_AUTO, TILE_128x128, TILE_128x224_CLUSTER2, TILE_128x256_CLUSTER2 = -1, 0, 1, 2
+TILE_128x128_CLUSTER2, TILE_128x160_CLUSTER2, TILE_128x192_CLUSTER2 = 3, 4, 5
+TILES = (0, 1, 2, 3, 4, 5)
 BSCALE_BLOCK_128x128, BSCALE_TILE_1x128 = 0, 1
 GROUP = 128
 

@@ -56,7 +56,7 @@ fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, co
     return FP8BS_ERR_INVALID_ARG;
   if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
   if (promote != 0 && promote != 1) return FP8BS_ERR_INVALID_ARG;
-  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_128x256_CLUSTER2) return FP8BS_ERR_INVALID_ARG;
+  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_128x192_CLUSTER2) return FP8BS_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FP8BS_OK;
   if (!a || !sa || !b || !sb || !c) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -179,10 +179,14 @@ const char* fp8bs_status_string(fp8bs_status s) {
 }
 
 fp8bs_status fp8bs_get_device_error(fp8bs_stream_t stream) {
-  unsigned int word = 0;
-  cudaError_t e = fp8bs::read_and_clear_device_error(as_cuda(stream), &word);
+  cudaError_t e = cudaStreamSynchronize(as_cuda(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  return word ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
+  unsigned int g = 0, q = 0;
+  e = fp8bs::read_and_clear_gemm_error(&g);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = fp8bs::read_and_clear_quant_error(&q);
+  if (e != cudaSuccess) return cuda_status(e);
+  return (g | q) ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
 }
 
 int fp8bs_last_cuda_error(void) { return t_last_cuda_error; }

@@ -14,6 +14,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "ptx.cuh"
+
 namespace fp8bs {
 
 constexpr int kGroup = 128;          // 1x128 tiles, 128x128 blocks
@@ -76,6 +78,27 @@ __device__ __forceinline__ float quotient_2step(float x, float s, float r) {
   float q1 = __fmaf_rn(e0, r, q0);
   float e1 = __fmaf_rn(-q1, s, x);
   return with_sign_of(__fmaf_rn(e1, r, q1), x);
+}
+
+// The same two steps for two elements of one group at once (packed FP32
+// pairs: each half rounded exactly as the scalar operations).  s * q is
+// written as q * (-s), which is the same exact product negated.
+__device__ __forceinline__ float2 quotient_1step_x2(float2 x, float s, float r) {
+  const float2 r2 = make_float2(r, r), ns2 = make_float2(-s, -s);
+  const float2 q0 = ptx::mul2_rn(x, r2);
+  const float2 e = ptx::fma2_rn(q0, ns2, x);
+  const float2 q = ptx::fma2_rn(e, r2, q0);
+  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
+}
+
+__device__ __forceinline__ float2 quotient_2step_x2(float2 x, float s, float r) {
+  const float2 r2 = make_float2(r, r), ns2 = make_float2(-s, -s);
+  const float2 q0 = ptx::mul2_rn(x, r2);
+  const float2 e0 = ptx::fma2_rn(q0, ns2, x);
+  const float2 q1 = ptx::fma2_rn(e0, r2, q0);
+  const float2 e1 = ptx::fma2_rn(q1, ns2, x);
+  const float2 q = ptx::fma2_rn(e1, r2, q1);
+  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
 }
 
 // General path for one element: exact division and every special case.

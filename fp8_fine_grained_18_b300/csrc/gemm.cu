@@ -108,8 +108,9 @@ struct Cfg {
   static_assert(CM == 1 || CM == 2, "CM");
   static constexpr int kBH = BN / CM;  // B rows this CTA loads (multicast when CM = 2)
   static_assert(kBH % 8 == 0, "B half must be whole 8-row swizzle atoms");
-  static constexpr int kTmemStride = BN <= 128 ? 128 : 256;  // columns between partials
-  static constexpr int kTBuf = 512 / kTmemStride;            // 4 or 2 partial buffers
+  // columns between TMEM partial buffers, and how many fit in 512 columns
+  static constexpr int kTmemStride = BN <= 128 ? 128 : BN <= 160 ? 160 : 256;
+  static constexpr int kTBuf = 512 / kTmemStride > 4 ? 4 : 512 / kTmemStride;
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
@@ -128,7 +129,7 @@ struct Cfg {
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
   static_assert(kAlloc <= kSmemLimit, "shared memory");
-  static constexpr bool kRegSplit = BN > 128;
+  static constexpr bool kRegSplit = BN > 128;  // accumulators above 64 per thread
 };
 
 template <int N>
@@ -137,12 +138,68 @@ __device__ __forceinline__ void reg_fence(uint32_t* r) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// Load step `st` (columns [32 st, 32 st + 32) of a warp's kHalf columns, or
-// the last 16 when kHalf is not a multiple of 32) from TMEM into r.
+// TMEM read steps of a promotion warp that owns kHalf columns: step st
+// covers columns [32 st, 32 st + width) of the warp's range, width = 32
+// except a final 16.  Every load starts on a multiple of 16 columns.
 template <int kHalf>
-__device__ __forceinline__ void tmem_ld_step(uint32_t taddr, int st, uint32_t* r) {
-  ptx::tmem_ld_32x32b_x16(taddr + st * 32, r);
-  if (st * 32 + 16 < kHalf) ptx::tmem_ld_32x32b_x16(taddr + st * 32 + 16, r + 16);
+struct PromoSteps {
+  static_assert(kHalf % 16 == 0, "columns");
+  static constexpr int kSteps = (kHalf + 31) / 32;
+  static constexpr int width(int st) { return kHalf - 32 * st < 32 ? kHalf - 32 * st : 32; }
+};
+
+// acc[a0 .. a0 + kC) += P * scale for one step of kC columns that starts at
+// column a0 of the warp's kHalf (tile column col0 + a0).  Block scales
+// change only at 128-column boundaries, which fall on multiples of 16
+// columns of the warp's range; tile scales change per column.
+template <int kC, int a0, bool B_TILE>
+__device__ __forceinline__ void promote_step(float* acc, const uint32_t* v, float sa_r,
+                                             const float* scb, int col0, float f_lo, float f_hi,
+                                             int a_split) {
+  if constexpr (B_TILE) {
+    // one broadcast 16-byte shared-memory read serves four columns
+    const float2 sa2 = make_float2(sa_r, sa_r);
+#pragma unroll
+    for (int j = 0; j < kC; j += 4) {
+      const float4 sb4 = *reinterpret_cast<const float4*>(scb + col0 + a0 + j);
+      const float2 p0 = make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+      const float2 p1 = make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+      const float2 r0 = ptx::fma2_rn(ptx::mul2_rn(p0, make_float2(sb4.x, sb4.y)), sa2,
+                                     make_float2(acc[a0 + j], acc[a0 + j + 1]));
+      const float2 r1 = ptx::fma2_rn(ptx::mul2_rn(p1, make_float2(sb4.z, sb4.w)), sa2,
+                                     make_float2(acc[a0 + j + 2], acc[a0 + j + 3]));
+      acc[a0 + j] = r0.x;
+      acc[a0 + j + 1] = r0.y;
+      acc[a0 + j + 2] = r1.x;
+      acc[a0 + j + 3] = r1.y;
+    }
+  } else {
+    // the warp's columns lie in at most two 128-column blocks: factor f_lo
+    // before column a_split of the warp's range, f_hi from there on (block
+    // boundaries fall on multiples of 16 columns)
+#pragma unroll
+    for (int j0 = 0; j0 < kC; j0 += 16) {
+      const float f = (a0 + j0 < a_split) ? f_lo : f_hi;
+      const float2 f2 = make_float2(f, f);
+#pragma unroll
+      for (int j = j0; j < j0 + 16 && j < kC; j += 2) {
+        const float2 pv = make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
+        const float2 r = ptx::fma2_rn(pv, f2, make_float2(acc[a0 + j], acc[a0 + j + 1]));
+        acc[a0 + j] = r.x;
+        acc[a0 + j + 1] = r.y;
+      }
+    }
+  }
+}
+
+// Load kC columns (32 or 16) from TMEM.
+template <int kC>
+__device__ __forceinline__ void tmem_ld_step(uint32_t taddr, uint32_t* r) {
+  static_assert(kC == 32 || kC == 16, "columns");
+  if constexpr (kC == 32)
+    ptx::tmem_ld_32x32b_x32(taddr, r);
+  else
+    ptx::tmem_ld_32x32b_x16(taddr, r);
 }
 
 template <int BN, int CM, bool PROMOTE, bool OUT_BF16, bool B_TILE>
@@ -153,10 +210,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int STAGES = L::kStages;
   constexpr int TBUF = L::kTBuf;
   constexpr int kHalf = BN / 2;         // columns per promotion warp
-  constexpr int kSteps = (kHalf + 31) / 32;  // 32-column TMEM load steps per K-group
-  // step 0 of every K-group uses staging buffer 0, so the last step of the
-  // previous K-group must use buffer 1
-  static_assert(kSteps % 2 == 0, "even number of TMEM load steps");
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kBM, BN);
   constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;  // bytes landing in this CTA
@@ -383,72 +436,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kHalf; ++j) acc[j] = 0.0f;
 
       if (PROMOTE) {
-        // Software pipeline over 32-column steps (kSteps per K-group): the
-        // TMEM load of step s+1 is issued right after step s's data has
-        // arrived and before step s's FMAs, so its latency hides behind
-        // them.  tcgen05.wait::ld waits for all of this thread's loads, which
-        // is why only one step is ever in flight.
-        uint32_t v[2][32];
-        uint32_t buf = kt % TBUF;
-        {
-          const uint32_t tph = (kt / TBUF) & 1;
-          bool w0 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
-          if (!__all_sync(0xFFFFFFFFu, w0)) { ok = false; break; }
-          ptx::tc_fence_after();
-          tmem_ld_step<kHalf>(tmem_base + t_lane + buf * L::kTmemStride + col0, 0, v[0]);
-        }
+        using PS = PromoSteps<kHalf>;
+        constexpr int kS = PS::kSteps;
+        static_assert(kS <= 4, "steps");
+        // Block scales: the first column of this warp's range that lies in
+        // the next 128-column block (kHalf when there is none).
+        const int a_split = B_TILE ? kHalf : ((n0 + col0) / 128 + 1) * 128 - (n0 + col0);
+        const int nb_lo = (n0 + col0) / 128 - n0 / 128;
         for (int kb = 0; kb < KB; ++kb, ++kt, ++ks) {
+          const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
           const uint32_t slot = ks % kScaleSlots, sph = (ks / kScaleSlots) & 1;
           bool w1 = wait_bar(&sfull[slot], sph, abort_flag, kErrPromo);
           if (!__all_sync(0xFFFFFFFFu, w1)) { ok = false; break; }
           const float* sc = sScale + slot * L::kScaleFloats;
           const float sa_r = sc[row];
           const float* scb = sc + kBM;
-          const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
-#pragma unroll
-          for (int st = 0; st < kSteps; ++st) {
-            ptx::tmem_ld_wait();
-            reg_fence<32>(v[st & 1]);
-            if (st + 1 < kSteps) {
-              tmem_ld_step<kHalf>(tcur, st + 1, v[(st + 1) & 1]);
-            } else {
-              // every TMEM read of this buffer is done: hand it back, then
-              // start on the next K-group's partial
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
-              if (kb + 1 < KB) {
-                const uint32_t kn = kt + 1;
-                buf = kn % TBUF;
-                bool w2 = wait_bar(&tfull[buf], (kn / TBUF) & 1, abort_flag, kErrPromo);
-                if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
-                ptx::tc_fence_after();
-                tmem_ld_step<kHalf>(tmem_base + t_lane + buf * L::kTmemStride + col0, 0,
-                                    v[0]);
-              }
-            }
-            const uint32_t* cur = v[st & 1];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int a0 = st * 32 + h * 16;  // accumulator index of this 16-column part
-              if (a0 >= kHalf) break;
-              const int cbase = col0 + a0;
-              if (B_TILE) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  const float f = __fmul_rn(sa_r, scb[cbase + j]);
-                  acc[a0 + j] = __fmaf_rn(__uint_as_float(cur[h * 16 + j]), f, acc[a0 + j]);
-                }
-              } else {
-                const int nbi = (n0 + cbase) / 128 - n0 / 128;
-                const float f = __fmul_rn(sa_r, scb[nbi]);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  acc[a0 + j] = __fmaf_rn(__uint_as_float(cur[h * 16 + j]), f, acc[a0 + j]);
-              }
-            }
+          float f_lo = 0.0f, f_hi = 0.0f;
+          if (!B_TILE) {
+            f_lo = __fmul_rn(sa_r, scb[nb_lo]);
+            f_hi = a_split < kHalf ? __fmul_rn(sa_r, scb[nb_lo + 1]) : f_lo;
           }
-          if (!ok) break;
+          bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
+          if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
+          ptx::tc_fence_after();
+          // Software pipeline over the K-group's TMEM read steps: the load of
+          // step s+1 is issued right after step s's data has arrived and
+          // before step s's FMAs.  tcgen05.wait::ld waits for all of this
+          // thread's loads, which is why only one step is ever in flight.
+          const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
+          uint32_t v[2][32];
+          tmem_ld_step<PS::width(0)>(tcur, v[0]);
+#define FP8BS_STEP(S)                                                                     \
+  if constexpr (S < kS) {                                                                 \
+    ptx::tmem_ld_wait();                                                                  \
+    reg_fence<PS::width(S)>(v[S & 1]);                                                    \
+    if constexpr (S + 1 < kS) {                                                           \
+      tmem_ld_step<PS::width(S + 1)>(tcur + 32 * (S + 1), v[(S + 1) & 1]);                \
+    } else {                                                                              \
+      /* every TMEM read of this buffer is done: hand it back */                          \
+      ptx::tc_fence_before();                                                             \
+      __syncwarp();                                                                       \
+      if (lane == 0) ptx::mbar_arrive(&tempty[buf]);                                      \
+    }                                                                                     \
+    promote_step<PS::width(S), 32 * S, B_TILE>(acc, v[S & 1], sa_r, scb, col0, f_lo, f_hi, \
+                                               a_split);                                  \
+  }
+          FP8BS_STEP(0)
+          FP8BS_STEP(1)
+          FP8BS_STEP(2)
+          FP8BS_STEP(3)
+#undef FP8BS_STEP
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sempty[slot]);
         }
@@ -539,39 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // Row-major uint8 matrix [rows][cols] (cols contiguous), box of box_rows x
 // 128 bytes with the 128-byte swizzle; out-of-range rows read as zero.
 bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols};
-  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return make_tmap_2d(map, base, 1, rows, cols, 128, box_rows, true);
 }
 
 constexpr int kMaxDevices = 64;
@@ -674,9 +682,18 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
 }
 
 // Tile shape per problem.  Each candidate's cost is the number of waves it
-// needs times its tile width over a relative efficiency (wider tiles and
-// clusters that share B tiles move fewer bytes per flop); the cheapest wins.
-enum TileShape { kTile128x128 = 0, kTile128x224x2 = 1, kTile128x256x2 = 2 };
+// needs times its tile width over a relative efficiency (measured per shape
+// on B300: wider tiles and clusters that share B tiles move fewer bytes per
+// flop; more TMEM partial buffers tolerate more promotion latency); the
+// cheapest wins.
+enum TileShape {
+  kTile128x128 = 0,
+  kTile128x224x2 = 1,
+  kTile128x256x2 = 2,
+  kTile128x128x2 = 3,
+  kTile128x160x2 = 4,
+  kTile128x192x2 = 5,
+};
 
 TileShape choose_tile(int64_t M, int64_t N, int sms) {
   struct Cand {
@@ -684,9 +701,9 @@ TileShape choose_tile(int64_t M, int64_t N, int sms) {
     int bn, cm;
     double eff;
   };
-  const Cand cands[] = {{kTile128x256x2, 256, 2, 1.0},
-                        {kTile128x224x2, 224, 2, 1.0},
-                        {kTile128x128, 128, 1, 0.7}};
+  const Cand cands[] = {{kTile128x256x2, 256, 2, 1.0}, {kTile128x224x2, 224, 2, 1.0},
+                        {kTile128x192x2, 192, 2, 0.9}, {kTile128x160x2, 160, 2, 0.9},
+                        {kTile128x128x2, 128, 2, 0.8}, {kTile128x128, 128, 1, 0.7}};
   TileShape best = kTile128x128;
   double best_cost = 1e300;
   const int64_t m_tiles = (M + kBM - 1) / kBM;
@@ -712,6 +729,12 @@ cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
       return launch_variant<256, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile128x224x2:
       return launch_variant<224, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile128x192x2:
+      return launch_variant<192, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile128x160x2:
+      return launch_variant<160, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile128x128x2:
+      return launch_variant<128, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     default:
       return launch_variant<128, 1, PROMOTE, OUT_BF16, B_TILE>(g, stream);
   }
@@ -734,12 +757,10 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   return g.promote ? launch_out<true>(g, stream) : launch_out<false>(g, stream);
 }
 
-cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word) {
+cudaError_t read_and_clear_gemm_error(unsigned int* word) {
   *word = 0;
-  cudaError_t e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) return e;
   unsigned int v = 0;
-  e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
   if (e != cudaSuccess) return e;
   if (v) {
     const unsigned int zero = 0;

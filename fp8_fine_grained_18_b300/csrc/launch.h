@@ -3,9 +3,16 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fp8bs {
+
+// Tensor map of a dense row-major matrix [rows][cols] of 1-, 2- or 4-byte
+// elements, box of box_cols x box_rows elements, optionally with the 128-byte
+// swizzle; out-of-range elements read as zero.  False if encoding failed.
+bool make_tmap_2d(CUtensorMap* map, const void* base, int elem_bytes, int64_t rows, int64_t cols,
+                  int box_cols, int box_rows, bool swizzle128);
 
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
                                    cudaStream_t stream);
@@ -32,8 +39,10 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
-// Reads and clears the device error word of the GEMM's bounded waits
-// (synchronizes the stream first).  *word = 0 when nothing timed out.
-cudaError_t read_and_clear_device_error(cudaStream_t stream, unsigned int* word);
+// Read and clear the device error words of the bounded waits in the GEMM
+// and in the quantizers (the caller synchronizes first).  *word = 0 when
+// nothing timed out.
+cudaError_t read_and_clear_gemm_error(unsigned int* word);
+cudaError_t read_and_clear_quant_error(unsigned int* word);
 
 }  // namespace fp8bs

@@ -4,66 +4,96 @@
 //   Q2  128x128 weight blocks (+ transposed copy)      (page P1, para 3)
 //   Q3  1x128 -> 128x1 re-tiling of cached FP8 codes   (page P1, para 3)
 //
-// All four read each input byte once and write each output byte once:
-// 16-byte coalesced global loads, group max-abs by integer max on the sign-
-// stripped bit patterns (monotone in |x| for non-NaN values; NaN patterns
-// sort above Inf, so one compare also detects "group holds Inf/NaN"), and
-// hardware E4M3x2 packing.  Groups that hold Inf/NaN, or whose scale is zero
-// or tiny, take the general per-element path with an exact division; all
-// others use the reciprocal-plus-correction quotient of fp8_common.cuh.
+// Q1 and Q2 are one streaming scheme: a persistent CTA per SM whose producer
+// warp moves input tiles into a ring of shared-memory stages with 2-D TMA
+// copies (mbarrier full/empty, every wait bounded), while 16 consumer warps
+// turn each stage into codes and scales and store them.  Where a tile's
+// threads must exchange group maxima, the consumers form two teams of 8
+// warps that work on alternate tiles, so one team's barrier waits overlap
+// the other's work.  Tiles are ordered with the K-group fastest, so the CTAs
+// running at one time read one contiguous band of the input.  Q1T and Q3,
+// which transpose, are plain one-tile-per-CTA kernels (see below).  Each
+// input byte is read from HBM once and each output byte written once.
+//
+// Group max-abs is an integer max on the sign-stripped bit patterns
+// (monotone in |x| for non-NaN values; NaN patterns sort above Inf, so one
+// compare also detects "group holds Inf/NaN"); only a tile that holds a NaN
+// recomputes its maxima with NaN excluded.  Codes are packed two at a time
+// by the hardware E4M3x2 converter.  Groups that hold Inf/NaN, or whose scale
+// is zero or tiny, take the general per-element path with an exact division;
+// all others use the reciprocal-plus-correction quotient of fp8_common.cuh.
 #include "fp8_common.cuh"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace fp8bs {
+
+__device__ unsigned int g_quant_error;  // set when a bounded wait gives up
 
 namespace {
 
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr uint32_t kBf16Inf = 0x7F80u;
 constexpr uint32_t kF32Inf = 0x7F800000u;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = 32 * kConsumerWarps;  // 512 consumer threads
+constexpr int kThreads = kConsumers + 32;        // + one producer warp
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s per wait
 
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
+// Max-abs on bf16 pairs: each 16-bit half keeps its own maximum magnitude
+// bit pattern (packed unsigned max).
+__device__ __forceinline__ uint32_t mag_pair_max(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
 }
 
-__device__ __forceinline__ uint32_t mag2_max(uint32_t acc, uint32_t w) {
-  acc = max(acc, w & 0x7FFFu);
-  return max(acc, (w >> 16) & 0x7FFFu);
+// The same with NaN patterns replaced by 0 (NaN is ignored by amax).
+__device__ __forceinline__ uint32_t mag_pair_max_no_nan(uint32_t acc, uint32_t w) {
+  const uint32_t m = w & 0x7FFF7FFFu;
+  const uint32_t lo = (m & 0xFFFFu) > kBf16Inf ? 0u : (m & 0xFFFFu);
+  const uint32_t hi = (m >> 16) > kBf16Inf ? 0u : (m >> 16);
+  return __vmaxu2(acc, lo | (hi << 16));
 }
 
-// Magnitude with NaN patterns replaced by 0 (NaN is ignored by amax).
-__device__ __forceinline__ uint32_t mag_no_nan(uint32_t m, uint32_t inf) {
-  return m > inf ? 0u : m;
+__device__ __forceinline__ uint32_t halves_max(uint32_t m) { return max(m & 0xFFFFu, m >> 16); }
+
+__device__ __forceinline__ bool pair_has_nan(uint32_t m) {
+  return (m & 0xFFFFu) > kBf16Inf || (m >> 16) > kBf16Inf;
 }
 
-__device__ __forceinline__ uint32_t mag2_max_no_nan(uint32_t acc, uint32_t w) {
-  acc = max(acc, mag_no_nan(w & 0x7FFFu, kBf16Inf));
-  return max(acc, mag_no_nan((w >> 16) & 0x7FFFu, kBf16Inf));
+// Max of |x| that propagates NaN (a NaN in the group shows up as NaN).
+__device__ __forceinline__ float fmax_abs_nan(float acc, float x) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(acc), "f"(fabsf(x)));
+  return r;
 }
 
-// Four bf16 pairs (one 16-byte vector) -> eight codes in two words.
 struct GroupScale {
   float s, r;
   bool fast;
 };
 
-__device__ __forceinline__ GroupScale make_scale(uint32_t mag_bf16_no_nan, bool special) {
+// Scale of a group from its amax given as a bit pattern (bf16 when bf16 is
+// true, else FP32); special = the group holds Inf or NaN.
+__device__ __forceinline__ GroupScale make_scale(uint32_t mag_no_nan_bits, bool special,
+                                                 bool bf16) {
   GroupScale g;
-  g.s = group_scale(__uint_as_float(mag_bf16_no_nan << 16));
+  g.s = group_scale(__uint_as_float(bf16 ? mag_no_nan_bits << 16 : mag_no_nan_bits));
   g.fast = !special && g.s >= kFastScaleMin;
   g.r = g.fast ? __frcp_rn(g.s) : 0.0f;
   return g;
 }
 
+// Two bf16 (one word, element 0 in the low half) -> two codes.
 __device__ __forceinline__ uint32_t codes_bf16x2(uint32_t w, const GroupScale& g) {
-  float a = bf16_lo(w), b = bf16_hi(w);
-  if (g.fast) return e4m3x2(quotient_1step(a, g.s, g.r), quotient_1step(b, g.s, g.r));
-  return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s));
+  const float2 x = make_float2(bf16_lo(w), bf16_hi(w));
+  if (g.fast) {
+    const float2 q = quotient_1step_x2(x, g.s, g.r);
+    return e4m3x2(q.x, q.y);
+  }
+  return e4m3x2_nan(quotient_general(x.x, g.s), quotient_general(x.y, g.s));
 }
 
+// Eight bf16 (one 16-byte vector) -> eight codes in two words.
 __device__ __forceinline__ uint2 codes_bf16x8(uint4 v, const GroupScale& g) {
   uint2 o;
   o.x = codes_bf16x2(v.x, g) | (codes_bf16x2(v.y, g) << 16);
@@ -71,70 +101,367 @@ __device__ __forceinline__ uint2 codes_bf16x8(uint4 v, const GroupScale& g) {
   return o;
 }
 
-// ---------------------------------------------------------------------------
-// Q1: 1x128 tiles.  CTA = 256 threads = 16 half-warps; a half-warp owns one
-// 128-element group (16 lanes x 8 bf16) of 4 rows; CTA tile 64 rows x one
-// K-group.  grid = (ceil(M/64), K/128).
-// ---------------------------------------------------------------------------
-constexpr int kQ1Rows = 64;
-
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(
-    const uint16_t* __restrict__ x, int64_t M, int64_t K, uint8_t* __restrict__ q,
-    float* __restrict__ s) {
-  const int64_t kb = blockIdx.y;
-  const int hw = threadIdx.x >> 4;
-  const int l16 = threadIdx.x & 15;
-  const int64_t row0 = (int64_t)blockIdx.x * kQ1Rows + hw;
-  const int64_t col = kb * kGroup + l16 * 8;
-
-  uint4 v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int64_t r = row0 + 16 * i;
-    v[i] = (r < M) ? ld_stream_v4(x + r * K + col) : make_uint4(0, 0, 0, 0);
+// Two FP32 values (full 24-bit significands) -> two codes.
+__device__ __forceinline__ uint32_t codes_f32x2(float a, float b, const GroupScale& g) {
+  if (g.fast) {
+    const float2 q = quotient_2step_x2(make_float2(a, b), g.s, g.r);
+    return e4m3x2(q.x, q.y);
   }
-  uint32_t mx[4];
-  bool special = false;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t m = 0;
-    m = mag2_max(m, v[i].x); m = mag2_max(m, v[i].y);
-    m = mag2_max(m, v[i].z); m = mag2_max(m, v[i].w);
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
-    mx[i] = m;
-    special |= (m >= kBf16Inf);
-  }
-  bool sp[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) sp[i] = mx[i] >= kBf16Inf;
-  if (__any_sync(kFull, special)) {  // warp-uniform: every lane shuffles
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t m = 0;
-      m = mag2_max_no_nan(m, v[i].x); m = mag2_max_no_nan(m, v[i].y);
-      m = mag2_max_no_nan(m, v[i].z); m = mag2_max_no_nan(m, v[i].w);
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
-      mx[i] = m;
+  return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s));
+}
+
+__device__ __forceinline__ GroupScale shfl_scale(const GroupScale& g, int src) {
+  GroupScale o;
+  o.s = __shfl_sync(kFull, g.s, src);
+  o.r = __shfl_sync(kFull, g.r, src);
+  o.fast = __shfl_sync(kFull, (int)g.fast, src) != 0;
+  return o;
+}
+
+// Bounded wait: false when it expired (the error word and the CTA's abort
+// flag get set) or another warp already aborted.
+__device__ __forceinline__ bool wait_q(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t addr = ptx::smem_addr(bar);
+#pragma unroll 1
+  for (int i = 0; i < 128; ++i)
+    if (ptx::mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (ptx::mbar_try_wait(addr, parity)) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      atomicOr(&g_quant_error, 1u);
+      return false;
     }
   }
+}
+
+// Consumer warp `warp` is done reading a stage.
+__device__ __forceinline__ void release_stage(uint64_t* empty, int lane) {
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(empty);
+}
+
+// The consumer warps that work on one tile together.
+struct Team {
+  int tid;           // thread index within the team
+  int warp;          // warp index within the team
+  int lane;
+  uint32_t bar;      // the team's named barrier
+  uint32_t threads;  // threads in the team
+  uint8_t* scratch;  // the team's shared-memory scratch
+  uint64_t* empty;   // empty barrier of the stage being consumed
+};
+
+// ---------------------------------------------------------------------------
+// Q1: 1x128 tiles.  Tile = 128 rows x one K-group (TMA box 128 x 128 bf16,
+// 32 KB).  Half-warp h (0..31) owns rows h, h + 32, h + 64, h + 96 of the
+// tile, each lane 8 consecutive elements of each; lanes 0..3 of the
+// half-warp compute the four groups' scales and share them by shuffle.
+// ---------------------------------------------------------------------------
+struct Q1 {
+  static constexpr int kRows = 128;
+  static constexpr int kStageBytes = kRows * 256;
+  static constexpr int kStages = 4;
+  static constexpr int kScratchBytes = 0;
+  static constexpr uint32_t kTx = kStageBytes;
+  static constexpr int kTeams = 1;
+  struct Params {
+    uint8_t* q;
+    float* s;
+    int M, K, KB, num_tiles;
+    const float* unused;
+  };
+  __device__ static void issue(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile,
+                               const Params& p) {
+    ptx::tma_load_2d(dst, map, bar, (tile % p.KB) * kGroup, (tile / p.KB) * kRows);
+  }
+  __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
+                                 const Team& tm) {
+    const int kb = tile % p.KB, rt = tile / p.KB;
+    const int lane = tm.lane;
+    const int hw = tm.warp * 2 + (lane >> 4);
+    const int l16 = lane & 15;
+    const uint4* st = reinterpret_cast<const uint4*>(stage);
+    uint4 v[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int64_t r = row0 + 16 * i;
-    if (r >= M) continue;
-    GroupScale g = make_scale(mx[i], sp[i]);
-    *reinterpret_cast<uint2*>(q + r * K + col) = codes_bf16x8(v[i], g);
-    if (l16 == 0) s[kb * M + r] = g.s;
+    for (int i = 0; i < 4; ++i) v[i] = st[(hw + 32 * i) * 16 + l16];
+    // per-row maxima, two rows packed per word, reduced over the half-warp
+    uint32_t m01 = 0, m23 = 0;
+    {
+      uint32_t a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        a[i] = halves_max(mag_pair_max(mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y),
+                                                    v[i].z),
+                                       v[i].w));
+      m01 = a[0] | (a[1] << 16);
+      m23 = a[2] | (a[3] << 16);
+    }
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+      m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
+      m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
+    }
+    const uint32_t plain01 = m01, plain23 = m23;
+    if (__any_sync(kFull, pair_has_nan(m01) || pair_has_nan(m23))) {  // recount without NaN
+      uint32_t a[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        a[i] = halves_max(mag_pair_max_no_nan(
+            mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
+                                v[i].z),
+            v[i].w));
+      m01 = a[0] | (a[1] << 16);
+      m23 = a[2] | (a[3] << 16);
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) {
+        m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
+        m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
+      }
+    }
+    release_stage(tm.empty, lane);
+    // lane j (0..3) of the half-warp computes row j's scale
+    const int j = l16 & 3;
+    const uint32_t mw = j < 2 ? m01 : m23, pw = j < 2 ? plain01 : plain23;
+    const uint32_t mj = (j & 1) ? (mw >> 16) : (mw & 0xFFFFu);
+    const uint32_t pj = (j & 1) ? (pw >> 16) : (pw & 0xFFFFu);
+    const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
+    const int64_t col = (int64_t)kb * kGroup + l16 * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const GroupScale g = shfl_scale(mine, (lane & 16) + i);
+      const int64_t r = (int64_t)rt * kRows + hw + 32 * i;
+      if (r < p.M) {
+        *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[i], g);
+        if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Q2: 128x128 weight blocks.  Tile = one block (TMA box 128 x 128 bf16,
+// 32 KB), one team of 256 threads.  Thread t holds elements (row, 8-column
+// segment) for idx = t + 256 j, row = idx / 16, segment = idx % 16; the
+// block max goes through shared memory.  The transposed copy is staged as a
+// code tile in the team's scratch and read back column-wise, 32 contiguous
+// bytes per thread.
+// ---------------------------------------------------------------------------
+struct Q2 {
+  static constexpr int kStageBytes = 128 * 256;
+  static constexpr int kStages = 4;
+  static constexpr int kTeamWarps = 8;
+  static constexpr int kScratchBytes = 128 * 128 + 2 * kTeamWarps * 4;
+  static constexpr uint32_t kTx = kStageBytes;
+  static constexpr int kTeams = 2;
+  struct Params {
+    uint8_t* q;
+    float* s;
+    uint8_t* qT;
+    float* sT;
+    int N, K, KB, NB, num_tiles;
+  };
+  __device__ static void issue(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile,
+                               const Params& p) {
+    ptx::tma_load_2d(dst, map, bar, (tile % p.KB) * kGroup, (tile / p.KB) * kGroup);
+  }
+  __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
+                                 const Team& tm) {
+    const int kb = tile % p.KB, nb = tile / p.KB;
+    const int t = tm.tid;
+    const uint4* st = reinterpret_cast<const uint4*>(stage);
+    uint2* ctile = reinterpret_cast<uint2*>(tm.scratch);
+    uint32_t* red = reinterpret_cast<uint32_t*>(tm.scratch + 128 * 128);
+    uint4 v[8];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = st[t + 256 * j];
+      m2 = mag_pair_max(mag_pair_max(mag_pair_max(mag_pair_max(m2, v[j].x), v[j].y), v[j].z),
+                        v[j].w);
+    }
+    release_stage(tm.empty, tm.lane);
+    uint32_t m = halves_max(m2);
+    const bool nan_here = m > kBf16Inf;
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
+    if (tm.lane == 0) red[tm.warp] = m;
+    const bool any_nan = ptx::named_barrier_or(tm.bar, tm.threads, nan_here);
+    uint32_t mp = 0;
+#pragma unroll
+    for (int i = 0; i < kTeamWarps; ++i) mp = max(mp, red[i]);
+    uint32_t mn = mp;
+    if (any_nan) {  // uniform: recount without NaN
+      uint32_t a2 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        a2 = mag_pair_max_no_nan(
+            mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(a2, v[j].x), v[j].y),
+                                v[j].z),
+            v[j].w);
+      uint32_t a = halves_max(a2);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) a = max(a, __shfl_xor_sync(kFull, a, off));
+      if (tm.lane == 0) red[kTeamWarps + tm.warp] = a;
+      ptx::named_barrier(tm.bar, tm.threads);
+      mn = 0;
+#pragma unroll
+      for (int i = 0; i < kTeamWarps; ++i) mn = max(mn, red[kTeamWarps + i]);
+    }
+    const GroupScale g = make_scale(mn, mp >= kBf16Inf, true);
+    const int64_t n0 = (int64_t)nb * kGroup, k0 = (int64_t)kb * kGroup;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int idx = t + 256 * j;
+      const uint2 cv = codes_bf16x8(v[j], g);
+      *reinterpret_cast<uint2*>(p.q + (n0 + (idx >> 4)) * p.K + k0 + (idx & 15) * 8) = cv;
+      if (p.qT) ctile[idx] = cv;
+    }
+    if (t == 0) {
+      p.s[(int64_t)nb * p.KB + kb] = g.s;
+      if (p.sT) p.sT[(int64_t)kb * p.NB + nb] = g.s;
+    }
+    if (p.qT) {
+      ptx::named_barrier(tm.bar, tm.threads);
+      const uint8_t* cb = reinterpret_cast<const uint8_t*>(ctile);
+      const int k = t & 127, h = t >> 7;  // output row k, rows h*64 .. h*64+63 of the block
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int n = h * 64 + half * 32 + 4 * i;
+          o[i] = (uint32_t)cb[n * 128 + k] | ((uint32_t)cb[(n + 1) * 128 + k] << 8) |
+                 ((uint32_t)cb[(n + 2) * 128 + k] << 16) | ((uint32_t)cb[(n + 3) * 128 + k] << 24);
+        }
+        uint4* d = reinterpret_cast<uint4*>(p.qT + (k0 + k) * p.N + n0 + h * 64 + half * 32);
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+};
+
+template <class Op>
+struct StreamSmem {
+  static constexpr int kRing = Op::kStages * Op::kStageBytes;
+  static constexpr int kScratchPerTeam = ((Op::kScratchBytes + 127) / 128) * 128;
+  static constexpr int kOffScratch = kRing;
+  static constexpr int kOffBars = kOffScratch + Op::kTeams * kScratchPerTeam;
+  static constexpr int kBytes = kOffBars + 2 * Op::kStages * 8 + 16;
+  static constexpr int kAlloc = kBytes + 128;  // room to align the base to 128
+  static_assert(Op::kStageBytes % 128 == 0, "stage alignment");
+  static_assert(Op::kStages <= 32, "stage mask");
+  // team t consumes the tiles at ring positions t, t + kTeams, ..., so each
+  // stage belongs to one team
+  static_assert(Op::kStages % Op::kTeams == 0, "stages per team");
+  static_assert(kConsumerWarps % Op::kTeams == 0, "warps per team");
+};
+
+// The streaming kernel: warp kConsumerWarps is the producer, warps
+// 0..kConsumerWarps-1 consume, in Op::kTeams teams.  CTA i handles tiles
+// i, i + grid, ...; its j-th tile goes to team j mod kTeams.
+template <class Op>
+__global__ void __launch_bounds__(kThreads, 1)
+    stream_kernel(const __grid_constant__ CUtensorMap map, const typename Op::Params p) {
+  using L = StreamSmem<Op>;
+  constexpr int S = Op::kStages;
+  constexpr int kTeamWarps = kConsumerWarps / Op::kTeams;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
+  uint64_t* empty = full + S;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], kTeamWarps);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&map);
+      uint32_t it = 0, issued = 0;
+      for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++it) {
+        const uint32_t s = it % S, ph = (it / S) & 1;
+        if (!wait_q(&empty[s], ph ^ 1, abort_flag)) break;
+        ptx::mbar_arrive_expect_tx(&full[s], Op::kTx);
+        Op::issue(&map, ring + s * Op::kStageBytes, &full[s], tile, p);
+        issued |= 1u << s;
+      }
+      // Drain: the last copy issued into each stage has landed before the
+      // CTA may exit (only the last phase of a stage can be in flight).
+      for (uint32_t s = 0; s < S; ++s) {
+        if (!((issued >> s) & 1u)) continue;
+        const uint32_t li = (it - 1) - (((it - 1) % S + S - s) % S);
+        const uint32_t addr = ptx::smem_addr(&full[s]);
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(addr, (li / S) & 1)) {
+          if (ptx::globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(&g_quant_error, 2u);
+            break;
+          }
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    const int team = warp / kTeamWarps;
+    Team tm;
+    tm.warp = warp % kTeamWarps;
+    tm.lane = lane;
+    tm.tid = tm.warp * 32 + lane;
+    tm.bar = 1 + team;
+    tm.threads = 32 * kTeamWarps;
+    tm.scratch = smem + L::kOffScratch + team * L::kScratchPerTeam;
+    uint32_t it = team;
+    for (int tile = blockIdx.x + team * gridDim.x; tile < p.num_tiles;
+         tile += Op::kTeams * gridDim.x, it += Op::kTeams) {
+      const uint32_t s = it % S, ph = (it / S) & 1;
+      const bool ok = wait_q(&full[s], ph, abort_flag);
+      // A team whose threads synchronize with each other decides together
+      // (this barrier also separates the previous tile's use of the team's
+      // scratch from this one's); single warps decide alone.
+      if (kTeamWarps > 1 && Op::kTeams > 1) {
+        if (ptx::named_barrier_or(tm.bar, tm.threads, !ok)) break;
+      } else {
+        if (!__all_sync(kFull, ok)) break;
+      }
+      tm.empty = &empty[s];
+      Op::consume(ring + s * Op::kStageBytes, tile, p, tm);
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Q1T: 128x1 tiles (groups of 128 consecutive rows of one column), output
-// transposed.  CTA tile = 128 rows x 128 columns staged in shared memory.
-// Thread (cp, p): column pair cp (0..63), rows p*32..p*32+31; a warp reads
-// 32 consecutive words of one row (conflict-free).  grid = (K/128, M/128).
+// The two transposing quantizers are plain kernels, one 128 x 128 tile per
+// CTA: 16-byte loads into a shared-memory tile, every thread reading words
+// along rows (conflict-free) and writing its codes as 16- or 32-byte runs of
+// the transposed output.
 // ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Q1T: 128x1 tiles (128 consecutive rows of one column), output transposed.
+// Thread (cp, part): column pair cp (0..63), rows 32 part .. 32 part + 31.
+// grid = (K/128, M/128).
 __global__ void __launch_bounds__(256) quant_act_128x1_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t K, uint8_t* __restrict__ qT,
     float* __restrict__ sT) {
@@ -144,57 +471,37 @@ __global__ void __launch_bounds__(256) quant_act_128x1_kernel(
   const int64_t k0 = (int64_t)blockIdx.x * kGroup;
   const int64_t mb = blockIdx.y;
   const int64_t m0 = mb * kGroup;
-
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    int idx = t + 256 * j;
-    int row = idx >> 4, g = idx & 15;
-    tile[idx] = ld_stream_v4(x + (m0 + row) * K + k0 + g * 8);
+    const int idx = t + 256 * j;
+    tile[idx] = ld_stream_v4(x + (m0 + (idx >> 4)) * K + k0 + (idx & 15) * 8);
   }
   __syncthreads();
-
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
-  const int cp = (t & 31) + 32 * ((t >> 5) & 1);
-  const int p = t >> 6;
-  uint32_t mlo = 0, mhi = 0;
+  const int cp = t & 63, part = t >> 6;
+  uint32_t m = 0;
 #pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
-    uint32_t w = tw[(p * 32 + i) * 64 + cp];
-    mlo = max(mlo, w & 0x7FFFu);
-    mhi = max(mhi, (w >> 16) & 0x7FFFu);
-  }
-  red[p][cp] = mlo | (mhi << 16);
+  for (int i = 0; i < 32; ++i) m = mag_pair_max(m, tw[(part * 32 + i) * 64 + cp]);
+  red[part][cp] = m;
   __syncthreads();
-  mlo = 0; mhi = 0;
+  uint32_t mp = 0;
 #pragma unroll
-  for (int pp = 0; pp < 4; ++pp) {
-    uint32_t w = red[pp][cp];
-    mlo = max(mlo, w & 0xFFFFu);
-    mhi = max(mhi, w >> 16);
+  for (int q = 0; q < 4; ++q) mp = __vmaxu2(mp, red[q][cp]);
+  uint32_t mn = mp;
+  if (pair_has_nan(mp)) {  // rare: recount this column pair without NaN
+    mn = 0;
+    for (int r = 0; r < 128; ++r) mn = mag_pair_max_no_nan(mn, tw[r * 64 + cp]);
   }
-  const bool sp_lo = mlo >= kBf16Inf, sp_hi = mhi >= kBf16Inf;
-  if (sp_lo || sp_hi) {  // rare: recount this column pair without NaN
-    uint32_t a = 0, b = 0;
-    for (int r = 0; r < 128; ++r) {
-      uint32_t w = tw[r * 64 + cp];
-      a = max(a, mag_no_nan(w & 0x7FFFu, kBf16Inf));
-      b = max(b, mag_no_nan((w >> 16) & 0x7FFFu, kBf16Inf));
-    }
-    mlo = a; mhi = b;
-  }
-  const GroupScale glo = make_scale(mlo, sp_lo);
-  const GroupScale ghi = make_scale(mhi, sp_hi);
-
+  const GroupScale glo = make_scale(mn & 0xFFFFu, (mp & 0xFFFFu) >= kBf16Inf, true);
+  const GroupScale ghi = make_scale(mn >> 16, (mp >> 16) >= kBf16Inf, true);
   uint32_t olo[8], ohi[8];
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
-    uint32_t w0 = tw[(p * 32 + i) * 64 + cp];
-    uint32_t w1 = tw[(p * 32 + i + 1) * 64 + cp];
-    // pack (row i, row i+1) of each column: low column from the low halves
-    uint32_t lo_pair = (w0 & 0xFFFFu) | (w1 << 16);
-    uint32_t hi_pair = (w0 >> 16) | (w1 & 0xFFFF0000u);
-    uint32_t clo = codes_bf16x2(lo_pair, glo);
-    uint32_t chi = codes_bf16x2(hi_pair, ghi);
+    const uint32_t w0 = tw[(part * 32 + i) * 64 + cp];
+    const uint32_t w1 = tw[(part * 32 + i + 1) * 64 + cp];
+    // (row i, row i + 1) of each column
+    const uint32_t clo = codes_bf16x2(__byte_perm(w0, w1, 0x5410), glo);
+    const uint32_t chi = codes_bf16x2(__byte_perm(w0, w1, 0x7632), ghi);
     if ((i & 2) == 0) {
       olo[i >> 2] = clo;
       ohi[i >> 2] = chi;
@@ -203,178 +510,90 @@ __global__ void __launch_bounds__(256) quant_act_128x1_kernel(
       ohi[i >> 2] |= chi << 16;
     }
   }
-  uint8_t* dlo = qT + (k0 + 2 * cp) * M + m0 + p * 32;
-  uint8_t* dhi = dlo + M;
-  reinterpret_cast<uint4*>(dlo)[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-  reinterpret_cast<uint4*>(dlo)[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
-  reinterpret_cast<uint4*>(dhi)[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-  reinterpret_cast<uint4*>(dhi)[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
-  if (p == 0)
+  uint4* dlo = reinterpret_cast<uint4*>(qT + (k0 + 2 * cp) * M + m0 + part * 32);
+  uint4* dhi = reinterpret_cast<uint4*>(qT + (k0 + 2 * cp + 1) * M + m0 + part * 32);
+  dlo[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+  dlo[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+  dhi[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+  dhi[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+  if (part == 0)
     *reinterpret_cast<float2*>(sT + mb * K + k0 + 2 * cp) = make_float2(glo.s, ghi.s);
 }
 
-// ---------------------------------------------------------------------------
-// Q2: one CTA per 128x128 weight block.  Each thread holds 64 elements
-// (8 x 16 bytes) in registers; the block max goes through shared memory.
-// The optional transposed copy is staged as a row-major code tile in shared
-// memory and read back column-wise (a warp reads 32 consecutive bytes).
-// grid = (K/128, N/128).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) quant_weight_128x128_kernel(
-    const uint16_t* __restrict__ w, int64_t N, int64_t K, uint8_t* __restrict__ q,
-    float* __restrict__ s, uint8_t* __restrict__ qT, float* __restrict__ sT) {
-  __shared__ uint2 ctile[128 * 16];  // codes, row n, 8-byte segment g at [n * 16 + g]
-  __shared__ uint32_t red[2][8];
-  const int t = threadIdx.x;
-  const int64_t kb = blockIdx.x, nb = blockIdx.y;
-  const int64_t KB = K / kGroup, NB = N / kGroup;
-  const int64_t n0 = nb * kGroup, k0 = kb * kGroup;
-
-  uint4 v[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    int idx = t + 256 * j;
-    v[j] = ld_stream_v4(w + (n0 + (idx >> 4)) * K + k0 + (idx & 15) * 8);
-  }
-  uint32_t m = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    m = mag2_max(m, v[j].x); m = mag2_max(m, v[j].y);
-    m = mag2_max(m, v[j].z); m = mag2_max(m, v[j].w);
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
-  if ((t & 31) == 0) red[0][t >> 5] = m;
-  __syncthreads();
-  m = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) m = max(m, red[0][i]);
-  const bool special = m >= kBf16Inf;  // block-uniform
-  if (special) {
-    m = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      m = mag2_max_no_nan(m, v[j].x); m = mag2_max_no_nan(m, v[j].y);
-      m = mag2_max_no_nan(m, v[j].z); m = mag2_max_no_nan(m, v[j].w);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
-    if ((t & 31) == 0) red[1][t >> 5] = m;
-    __syncthreads();
-    m = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = max(m, red[1][i]);
-  }
-  const GroupScale g = make_scale(m, special);
-
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    int idx = t + 256 * j;
-    uint2 c = codes_bf16x8(v[j], g);
-    *reinterpret_cast<uint2*>(q + (n0 + (idx >> 4)) * K + k0 + (idx & 15) * 8) = c;
-    if (qT) ctile[idx] = c;
-  }
-  if (t == 0) {
-    s[nb * KB + kb] = g.s;
-    if (sT) sT[kb * NB + nb] = g.s;
-  }
-  if (qT) {
-    __syncthreads();
-    const uint8_t* cb = reinterpret_cast<const uint8_t*>(ctile);
-    const int k = t & 127, h = t >> 7;
-    uint32_t o[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int n = h * 64 + 4 * i;
-      o[i] = (uint32_t)cb[n * 128 + k] | ((uint32_t)cb[(n + 1) * 128 + k] << 8) |
-             ((uint32_t)cb[(n + 2) * 128 + k] << 16) | ((uint32_t)cb[(n + 3) * 128 + k] << 24);
-    }
-    uint4* d = reinterpret_cast<uint4*>(qT + (k0 + k) * N + n0 + h * 64);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Q3: 1x128 -> 128x1.  CTA tile = 128 rows (one 128-token group) x 128
-// columns (one K-group) of codes plus their 128 row scales, in shared
-// memory.  Thread (cq, p): columns 4cq..4cq+3, rows p*16..p*16+15.
-// x_hat = decode(code) * s_row (one RN multiply), then the column groups are
-// quantized again and written transposed.  grid = (K/128, M/128).
-// ---------------------------------------------------------------------------
+// Four codes (one word) of one row, dequantized with that row's scale:
+// x_hat = decode(code) * s, one round-to-nearest multiply each.
 __device__ __forceinline__ void dequant4(uint32_t w, float s, float (&o)[4]) {
-  float2 a = e4m3x2_decode(w & 0xFFFFu);
-  float2 b = e4m3x2_decode(w >> 16);
-  o[0] = __fmul_rn(a.x, s); o[1] = __fmul_rn(a.y, s);
-  o[2] = __fmul_rn(b.x, s); o[3] = __fmul_rn(b.y, s);
+  const float2 s2 = make_float2(s, s);
+  const float2 a = ptx::mul2_rn(e4m3x2_decode(w & 0xFFFFu), s2);
+  const float2 b = ptx::mul2_rn(e4m3x2_decode(w >> 16), s2);
+  o[0] = a.x;
+  o[1] = a.y;
+  o[2] = b.x;
+  o[3] = b.y;
 }
 
+// Q3: 1x128 -> 128x1.  CTA tile = 128 rows (one 128-token group) x 128
+// columns (one K-group) of codes plus their 128 row scales.  Thread
+// (cq, part): columns 4 cq .. 4 cq + 3, rows 16 part .. 16 part + 15; the
+// values are dequantized once for the column maxima (float maxima that
+// propagate NaN; a column holding a NaN recounts without it) and again for
+// the codes.  grid = (K/128, M/128).
 __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t M, int64_t K,
     uint8_t* __restrict__ qT, float* __restrict__ sT) {
   __shared__ uint4 tile[128 * 8];  // row r, 16-byte segment g at [r * 8 + g]
   __shared__ float srow[128];
-  __shared__ uint32_t red[8][128];
+  __shared__ float red[8][128];
   const int t = threadIdx.x;
   const int64_t kb = blockIdx.x, mb = blockIdx.y;
   const int64_t k0 = kb * kGroup, m0 = mb * kGroup;
-
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    int idx = t + 256 * j;
+    const int idx = t + 256 * j;
     tile[idx] = ld_stream_v4(q + (m0 + (idx >> 3)) * K + k0 + (idx & 7) * 16);
   }
   if (t < 128) srow[t] = s[kb * M + m0 + t];
   __syncthreads();
-
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
-  const int cq = t & 31, p = t >> 5;
-  uint32_t mx[4] = {0, 0, 0, 0};
+  const int cq = t & 31, part = t >> 5;
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
   for (int i = 0; i < 16; ++i) {
-    const int r = p * 16 + i;
+    const int r = part * 16 + i;
     float xv[4];
     dequant4(tw[r * 32 + cq], srow[r], xv);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) mx[c] = max(mx[c], __float_as_uint(xv[c]) & 0x7FFFFFFFu);
+    for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xv[c]);
   }
-#pragma unroll
-  for (int c = 0; c < 4; ++c) red[p][4 * cq + c] = mx[c];
+  *reinterpret_cast<float4*>(&red[part][4 * cq]) = make_float4(m[0], m[1], m[2], m[3]);
   __syncthreads();
   GroupScale g[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t m = 0;
+    float mp = 0.0f;  // NaN if the column holds a NaN
 #pragma unroll
-    for (int pp = 0; pp < 8; ++pp) m = max(m, red[pp][4 * cq + c]);
-    const bool special = m >= kF32Inf;
-    if (special) {  // rare: recount this column without NaN
-      m = 0;
+    for (int pp = 0; pp < 8; ++pp) mp = fmax_abs_nan(mp, red[pp][4 * cq + c]);
+    float mn = mp;
+    if (mp != mp) {  // rare: recount this column ignoring NaN
+      mn = 0.0f;
       for (int r = 0; r < 128; ++r) {
         float xv[4];
         dequant4(tw[r * 32 + cq], srow[r], xv);
-        m = max(m, mag_no_nan(__float_as_uint(xv[c]) & 0x7FFFFFFFu, kF32Inf));
+        mn = fmaxf(mn, fabsf(xv[c]));
       }
     }
-    g[c].s = group_scale(__uint_as_float(m));
-    g[c].fast = !special && g[c].s >= kFastScaleMin;
-    g[c].r = g[c].fast ? __frcp_rn(g[c].s) : 0.0f;
+    g[c] = make_scale(__float_as_uint(mn), !(mp < __uint_as_float(kF32Inf)), false);
   }
-
   uint32_t o[4][4];
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
-    const int r = p * 16 + i;
+    const int r = part * 16 + i;
     float x0[4], x1[4];
     dequant4(tw[r * 32 + cq], srow[r], x0);
     dequant4(tw[(r + 1) * 32 + cq], srow[r + 1], x1);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t code;
-      if (g[c].fast)
-        code = e4m3x2(quotient_2step(x0[c], g[c].s, g[c].r), quotient_2step(x1[c], g[c].s, g[c].r));
-      else
-        code = e4m3x2_nan(quotient_general(x0[c], g[c].s), quotient_general(x1[c], g[c].s));
+      const uint32_t code = codes_f32x2(x0[c], x1[c], g[c]);
       if ((i & 2) == 0)
         o[c][i >> 2] = code;
       else
@@ -383,19 +602,48 @@ __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(qT + (k0 + 4 * cq + c) * M + m0 + p * 16) =
+    *reinterpret_cast<uint4*>(qT + (k0 + 4 * cq + c) * M + m0 + part * 16) =
         make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
-  if (p == 0)
-    *reinterpret_cast<float4*>(sT + mb * K + k0 + 4 * cq) = make_float4(g[0].s, g[1].s, g[2].s, g[3].s);
+  if (part == 0)
+    *reinterpret_cast<float4*>(sT + mb * K + k0 + 4 * cq) =
+        make_float4(g[0].s, g[1].s, g[2].s, g[3].s);
+}
+
+int num_sms_current_device() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <class Op>
+cudaError_t launch_stream(const CUtensorMap& map, const typename Op::Params& p,
+                          cudaStream_t stream) {
+  using L = StreamSmem<Op>;
+  auto kern = stream_kernel<Op>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  int grid = num_sms_current_device();
+  if (grid > p.num_tiles) grid = p.num_tiles;
+  kern<<<grid, kThreads, L::kAlloc, stream>>>(map, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
                                    cudaStream_t stream) {
-  dim3 grid((unsigned)((M + kQ1Rows - 1) / kQ1Rows), (unsigned)(K / kGroup));
-  quant_act_1x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K, q, s);
-  return cudaGetLastError();
+  CUtensorMap map;
+  if (!make_tmap_2d(&map, x, 2, M, K, kGroup, Q1::kRows, false)) return cudaErrorInvalidValue;
+  Q1::Params p;
+  p.q = q;
+  p.s = s;
+  p.M = (int)M;
+  p.K = (int)K;
+  p.KB = (int)(K / kGroup);
+  p.num_tiles = (int)((M + Q1::kRows - 1) / Q1::kRows) * p.KB;
+  p.unused = nullptr;
+  return launch_stream<Q1>(map, p, stream);
 }
 
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t* qT, float* sT,
@@ -407,10 +655,19 @@ cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t*
 
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
                                         uint8_t* qT, float* sT, cudaStream_t stream) {
-  dim3 grid((unsigned)(K / kGroup), (unsigned)(N / kGroup));
-  quant_weight_128x128_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(w), N, K, q,
-                                                        s, qT, sT);
-  return cudaGetLastError();
+  CUtensorMap map;
+  if (!make_tmap_2d(&map, w, 2, N, K, kGroup, kGroup, false)) return cudaErrorInvalidValue;
+  Q2::Params p;
+  p.q = q;
+  p.s = s;
+  p.qT = qT;
+  p.sT = sT;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.KB = (int)(K / kGroup);
+  p.NB = (int)(N / kGroup);
+  p.num_tiles = p.NB * p.KB;
+  return launch_stream<Q2>(map, p, stream);
 }
 
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
@@ -418,6 +675,20 @@ cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int6
   dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
   requant_1x128_to_128x1_kernel<<<grid, 256, 0, stream>>>(q, s, M, K, qT, sT);
   return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_quant_error(unsigned int* word) {
+  *word = 0;
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = v;
+  return cudaSuccess;
 }
 
 }  // namespace fp8bs

@@ -159,14 +159,17 @@ fp8bs_status fp8bs_gemm_ex(const uint8_t *a, const float *sa,
  * problem, the shape that needs the fewest full waves of tiles over the
  * device's SMs, weighted by each shape's efficiency.
  *   128x128            one CTA per tile;
- *   128x224, 128x256   clusters of two CTAs on vertically adjacent tiles
+ *   128xBN_CLUSTER2    clusters of two CTAs on vertically adjacent tiles
  *                      that share (and multicast) the B tile.
  */
 typedef enum {
   FP8BS_TILE_AUTO = -1,
   FP8BS_TILE_128x128 = 0,
   FP8BS_TILE_128x224_CLUSTER2 = 1,
-  FP8BS_TILE_128x256_CLUSTER2 = 2
+  FP8BS_TILE_128x256_CLUSTER2 = 2,
+  FP8BS_TILE_128x128_CLUSTER2 = 3,
+  FP8BS_TILE_128x160_CLUSTER2 = 4,
+  FP8BS_TILE_128x192_CLUSTER2 = 5
 } fp8bs_tile_shape;
 
 /*

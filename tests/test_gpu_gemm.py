@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 BLOCK, TILE = 0, 1
 # every output-tile shape of the kernel (the automatic choice differs by shape)
-TILES = [0, 1, 2]
+TILES = [0, 1, 2, 3, 4, 5]
 
 
 def _quantized_pair(oracle_mod, M, N, K, seed, bkind):
