@@ -41,9 +41,10 @@ FP8_OVER_BF16 = 2.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM traffic of one GEMM launch on the dense workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
-# source it was taken on; None until captured.
-TRAFFIC = {"gemm": None}
+# (dram__bytes_read.sum + dram__bytes_write.sum; profiles/dense_fprop_step_ncu.md),
+# valid only for the kernel source it was taken on (sha of gemm.cu, ptx.cuh,
+# fp8_common.cuh); reported as null once the source has changed.
+TRAFFIC = {"gemm": {"bytes": 87100416 + 35971840, "src_sha": "28097afd7fceded8"}}
 
 
 def kernel_source_sha():
@@ -66,29 +67,37 @@ def load_peaks():
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running."""
+    """Samples the SM clock and the clock-event reasons while the timed
+    region runs: through NVML (pynvml) when it is importable, otherwise by
+    running `nvidia-smi --query-gpu ... -lms 50` beside the loop."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.active"]
 
     def __init__(self, torch_device):
-        self.samples, self.reasons, self.ok, self.err = [], set(), False, None
+        self.samples, self.reasons, self.err = [], set(), None
         self._stop = threading.Event()
         self.max_mhz = None
+        self.index = int(torch_device)
+        self.mode = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(int(torch_device))
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
             self._reasons_fn = fn or pynvml.nvmlDeviceGetCurrentClocksThrottleReasons
-            self.ok = True
-        except Exception as e:  # noqa: BLE001 -- reported in the JSON line
-            self.err = f"{type(e).__name__}: {e}"
+            self.mode = "nvml"
+        except Exception as e:  # noqa: BLE001 -- fall back to nvidia-smi
+            self.err = f"nvml: {type(e).__name__}: {e}"
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
@@ -102,23 +111,78 @@ class ClockSampler:
             time.sleep(0.005)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        elif self.mode == "smi":
+            import subprocess
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif self.mode == "smi":
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            for line in out.splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) != 3:
+                    continue
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                    r = int(parts[2], 16)
+                except ValueError:
+                    continue
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
 
     def summary(self):
         out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
-               "samples": len(self.samples), "source": "NVML, 5 ms polling"}
-        if self.err:
+               "samples": len(self.samples),
+               "source": {"nvml": "NVML, 5 ms polling", "smi": "nvidia-smi -lms 50",
+                          None: "unavailable"}[self.mode]}
+        if self.err and not self.samples:
             out["error"] = self.err
         return out
+
+
+# ------------------------------------------------------- multi-rank logic
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s batch: rank 0 draws the workload's own batch,
+    every other rank an independent batch of the same distribution (weak
+    scaling: each rank quantizes and multiplies its own tokens)."""
+    return base_seed if rank == 0 else base_seed + 1000 * rank
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); the
+    value itself when not distributed."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, world: int, steps: int, max_ms: float) -> float:
+    """Units per second over the whole job: every rank's units over the
+    slowest rank's time."""
+    return world * units_per_rank_step * steps / (max_ms * 1e-3)
 
 
 # ---------------------------------------------------------------- our arm
@@ -151,7 +215,7 @@ def run_ours(args):
 
     w = synth.WORKLOADS[WORKLOAD]
     M, N, K = w.M, w.N, w.K
-    inp = synth.make_inputs(WORKLOAD)
+    inp = synth.make_inputs(WORKLOAD, seed=rank_seed(w.seed, rank))
     a_host = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16)
     b_host = torch.from_numpy(inp["B"].view(np.int16)).view(torch.bfloat16)
     a = a_host.to(dev)
@@ -202,13 +266,9 @@ def run_ours(args):
     t_q2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     t_g = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
     t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
-    total_ms = sum(t_step)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(t_step), dist, dev)
     flops = 2.0 * M * N * K
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(flops, world, args.steps, total_ms) / 1e12
     ms_per_step = total_ms / args.steps
 
     # roofline of the dominant kernel (the GEMM)
@@ -256,12 +316,8 @@ def run_ours(args):
         c_pin.copy_(c, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e = {"value": round(whole_job_rate(flops, world, 1, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": a.numel() * 2 + b.numel() * 2,
            "d2h_bytes_per_step": c.numel() * 2, "ms_per_step": round(e2e_ms, 3)}
 

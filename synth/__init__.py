@@ -83,16 +83,17 @@ WORKLOADS = {
 }
 
 
-def make_inputs(name: str, scale_rows: int = None) -> dict:
+def make_inputs(name: str, scale_rows: int = None, seed: int = None) -> dict:
     """bf16 bit arrays of a workload.
 
     Forward workloads return {"A": [M, K], "B": [N, K]}; "bwd" returns
     {"X": [M, K], "W": [N, K], "dY": [M, N]} with M tokens, N output
     features, K input features.  scale_rows, if given, replaces M (the token
-    count) to draw a smaller batch of the same distribution.
+    count) to draw a smaller batch of the same distribution; seed, if given,
+    replaces the workload's seed (another batch of the same distribution).
     """
     w = WORKLOADS[name]
-    rng = np.random.default_rng(w.seed)
+    rng = np.random.default_rng(w.seed if seed is None else seed)
     M = w.M if scale_rows is None else scale_rows
     if name == "tiny":
         A, _ = normal_with_outlier_columns(rng, (M, w.K), 4, 50.0)
