@@ -48,57 +48,37 @@ __device__ __forceinline__ float2 e4m3x2_decode(uint32_t two_codes) {
 // Scale of a group whose max magnitude is amax.
 __device__ __forceinline__ float group_scale(float amax) { return __fdiv_rn(amax, kE4M3Max); }
 
-// Fast path: a normal, finite scale.  r must be the correctly rounded
-// reciprocal of s.  One Markstein correction step (P. Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", 1990):
-// q0 = x*r, e = x - s*q0 (exact), q = q0 + e*r, each rounded once.  For the
-// bf16 inputs of the activation and weight quantizers it reproduces the IEEE
-// quotient fl32(x/s) wherever the quotient is >= 2^-12 (checked exhaustively
-// over all bf16 significand pairs and exponent gaps); below that every
-// candidate codes as a signed zero.
-// The correction adds a zero of either sign for x = +-0 and may produce +0
-// for a negative quotient that underflows, so x's sign is put back: for a
-// positive scale the quotient's sign is always x's sign.
-__device__ __forceinline__ float with_sign_of(float q, float x) {
-  return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
-}
-
-__device__ __forceinline__ float quotient_1step(float x, float s, float r) {
-  float q0 = __fmul_rn(x, r);
-  float e = __fmaf_rn(-q0, s, x);
-  return with_sign_of(__fmaf_rn(e, r, q0), x);
+// Fast path: a normal, finite scale s with nr = -fl32(1/s) (a correctly
+// rounded reciprocal, negated).  The quotient is formed negated, by one
+// Markstein correction step (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", 1990) with every
+// operation rounded once:
+//   Q0 = x * nr,  e = fma(Q0, s, x) (= x - s * q0, exact),  Q = fma(e, nr, Q0)
+// which is -fl32(x / s): round-to-nearest is symmetric under negation, and
+// in this arrangement a zero quotient also comes out with the opposite of
+// x's sign, so -Q carries x's sign in every case.  The caller converts Q to
+// E4M3 and flips the sign bit of each code.  For the bf16 inputs of the
+// activation and weight quantizers one step reproduces fl32(x/s) wherever
+// |x/s| >= 2^-12 (checked exhaustively over bf16 inputs against IEEE
+// division); below that every candidate codes as a zero of x's sign.
+// Two packed FP32 lanes are processed per instruction.
+__device__ __forceinline__ float2 neg_quotient_1step_x2(float2 x, float s, float nr) {
+  const float2 nr2 = make_float2(nr, nr), s2 = make_float2(s, s);
+  const float2 q0 = ptx::mul2_rn(x, nr2);
+  const float2 e = ptx::fma2_rn(q0, s2, x);
+  return ptx::fma2_rn(e, nr2, q0);
 }
 
 // Two correction steps: the first makes the quotient faithful for any FP32
 // x, the second then yields the correctly rounded quotient (Markstein's
 // theorem).  Used where x is a full 24-bit FP32 value (the requantizer).
-__device__ __forceinline__ float quotient_2step(float x, float s, float r) {
-  float q0 = __fmul_rn(x, r);
-  float e0 = __fmaf_rn(-q0, s, x);
-  float q1 = __fmaf_rn(e0, r, q0);
-  float e1 = __fmaf_rn(-q1, s, x);
-  return with_sign_of(__fmaf_rn(e1, r, q1), x);
-}
-
-// The same two steps for two elements of one group at once (packed FP32
-// pairs: each half rounded exactly as the scalar operations).  s * q is
-// written as q * (-s), which is the same exact product negated.
-__device__ __forceinline__ float2 quotient_1step_x2(float2 x, float s, float r) {
-  const float2 r2 = make_float2(r, r), ns2 = make_float2(-s, -s);
-  const float2 q0 = ptx::mul2_rn(x, r2);
-  const float2 e = ptx::fma2_rn(q0, ns2, x);
-  const float2 q = ptx::fma2_rn(e, r2, q0);
-  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
-}
-
-__device__ __forceinline__ float2 quotient_2step_x2(float2 x, float s, float r) {
-  const float2 r2 = make_float2(r, r), ns2 = make_float2(-s, -s);
-  const float2 q0 = ptx::mul2_rn(x, r2);
-  const float2 e0 = ptx::fma2_rn(q0, ns2, x);
-  const float2 q1 = ptx::fma2_rn(e0, r2, q0);
-  const float2 e1 = ptx::fma2_rn(q1, ns2, x);
-  const float2 q = ptx::fma2_rn(e1, r2, q1);
-  return make_float2(with_sign_of(q.x, x.x), with_sign_of(q.y, x.y));
+__device__ __forceinline__ float2 neg_quotient_2step_x2(float2 x, float s, float nr) {
+  const float2 nr2 = make_float2(nr, nr), s2 = make_float2(s, s);
+  const float2 q0 = ptx::mul2_rn(x, nr2);
+  const float2 e0 = ptx::fma2_rn(q0, s2, x);
+  const float2 q1 = ptx::fma2_rn(e0, nr2, q0);
+  const float2 e1 = ptx::fma2_rn(q1, s2, x);
+  return ptx::fma2_rn(e1, nr2, q1);
 }
 
 // General path for one element: exact division and every special case.

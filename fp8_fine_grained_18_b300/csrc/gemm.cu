@@ -52,18 +52,10 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 128;            // one scale group per pipeline stage
-constexpr int kThreads = 384;       // 12 warps
-constexpr int kFirstPromoWarp = 4;  // warps 4..11
-constexpr int kPromoWarps = 8;
+constexpr int kFirstPromoWarp = 4;  // warps 0..3 control, 4.. promotion
 constexpr int kScaleSlots = 8;
 constexpr int kSmemLimit = 232448;  // 227 KB: the opt-in maximum per block
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
-// Register split when the accumulators need more than an even share:
-// warpgroup 0 (producer, MMA, scales) keeps kCtlRegs, the two promotion
-// warpgroups get kPromoRegs.  Their sum must fit in what the launch holds.
-constexpr int kCtlRegs = 40;
-constexpr int kPromoRegs = 232;
-constexpr int kSplitRegsNeeded = 128 * kCtlRegs + 256 * kPromoRegs;
 
 enum : unsigned int {
   kErrProducer = 1u,
@@ -102,17 +94,39 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-template <int BN, int CM>
+// PW promotion warps (8 or 12) share the tile's columns: each owns 32 TMEM
+// lanes (rows) and kCols = BN / (PW / 4) columns.
+template <int BN, int CM, bool PAIR, int PW>
 struct Cfg {
+  static_assert(PW == 8 || PW == 12, "promotion warps");
+  static constexpr int kPromoWarps = PW;
+  static constexpr int kThreads = 32 * (kFirstPromoWarp + PW);
+  static constexpr int kCols = BN / (PW / 4);
+  static_assert(kCols % 16 == 0, "columns per promotion warp");
+  // A warp with at most 64 columns reads its whole partial from TMEM at once
+  // and hands the buffer back before its FMAs; wider warps read in steps.
+  static constexpr bool kLoadAll = kCols <= 64;
+  // Register split when the accumulators need more than an even share:
+  // warpgroup 0 (producer, MMA, scales) keeps kCtlRegs, the promotion
+  // warpgroups get kPromoRegs.  Their sum must fit in what the launch holds
+  // (65536 registers, kThreads threads).
+  static constexpr bool kRegSplit = PW == 12 || BN > 128;
+  static constexpr int kCtlRegs = PW == 12 ? 56 : 40;
+  static constexpr int kPromoRegs = PW == 12 ? 152 : 232;
+  static constexpr int kSplitRegsNeeded = 128 * kCtlRegs + 32 * PW * kPromoRegs;
+  static_assert(!kRegSplit || kSplitRegsNeeded <= 65536, "register split");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(CM == 1 || CM == 2, "CM");
-  static constexpr int kBH = BN / CM;  // B rows this CTA loads (multicast when CM = 2)
+  static_assert(!PAIR || CM == 2, "a CTA pair is a cluster of two");
+  // B rows this CTA loads: multicast to both CTAs when CM = 2, or, for a CTA
+  // pair, its own half of the pair's B tile
+  static constexpr int kBH = BN / CM;
   static_assert(kBH % 8 == 0, "B half must be whole 8-row swizzle atoms");
   // columns between TMEM partial buffers, and how many fit in 512 columns
   static constexpr int kTmemStride = BN <= 128 ? 128 : BN <= 160 ? 160 : 256;
   static constexpr int kTBuf = 512 / kTmemStride > 4 ? 4 : 512 / kTmemStride;
   static constexpr int kABytes = kBM * kBK;
-  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kBBytes = (PAIR ? kBH : BN) * kBK;
   static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
   static constexpr int kScaleFloats = kBM + kScaleB;
   static constexpr int kNumBarsMax = 2 * 8 + 2 * 4 + 2 * kScaleSlots + 1;
@@ -129,8 +143,45 @@ struct Cfg {
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
   static_assert(kAlloc <= kSmemLimit, "shared memory");
-  static constexpr bool kRegSplit = BN > 128;  // accumulators above 64 per thread
 };
+
+// The four K = 32 MMAs of one K-group (accumulating onto D unless this is
+// the first K-group and `accumulate_first` is false).
+template <bool PAIR>
+__device__ __forceinline__ void issue_kgroup(uint32_t d, uint32_t a0, uint32_t b0, uint32_t idesc,
+                                             bool accumulate_first) {
+#pragma unroll
+  for (int k = 0; k < kBK / 32; ++k) {
+    const uint64_t ad = ptx::smem_desc_k128_sw128(a0 + 32 * k);
+    const uint64_t bd = ptx::smem_desc_k128_sw128(b0 + 32 * k);
+    const uint32_t acc = (accumulate_first || k > 0) ? 1u : 0u;
+    if (PAIR)
+      ptx::mma_f8f6f4_pair(d, ad, bd, idesc, acc);
+    else
+      ptx::mma_f8f6f4(d, ad, bd, idesc, acc);
+  }
+}
+
+// Free a shared-memory stage once the MMAs reading it completed: in this
+// CTA, in both CTAs of a multicast cluster, or in both CTAs of a pair.
+template <int CM, bool PAIR>
+__device__ __forceinline__ void commit_stage(uint64_t* empty, uint16_t peers) {
+  if (PAIR)
+    ptx::tc_commit_pair_mcast(empty, peers);
+  else if (CM == 1)
+    ptx::tc_commit(empty);
+  else
+    ptx::tc_commit_mcast(empty, peers);
+}
+
+// Hand a TMEM partial buffer back to the MMA issuer (the pair's leader).
+template <bool PAIR>
+__device__ __forceinline__ void release_tmem(uint64_t* tempty) {
+  if (PAIR)
+    ptx::mbar_arrive_cluster(ptx::mapa(tempty, 0));
+  else
+    ptx::mbar_arrive(tempty);
+}
 
 template <int N>
 __device__ __forceinline__ void reg_fence(uint32_t* r) {
@@ -138,18 +189,18 @@ __device__ __forceinline__ void reg_fence(uint32_t* r) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// TMEM read steps of a promotion warp that owns kHalf columns: step st
+// TMEM read steps of a promotion warp that owns kCols columns: step st
 // covers columns [32 st, 32 st + width) of the warp's range, width = 32
 // except a final 16.  Every load starts on a multiple of 16 columns.
-template <int kHalf>
+template <int kCols>
 struct PromoSteps {
-  static_assert(kHalf % 16 == 0, "columns");
-  static constexpr int kSteps = (kHalf + 31) / 32;
-  static constexpr int width(int st) { return kHalf - 32 * st < 32 ? kHalf - 32 * st : 32; }
+  static_assert(kCols % 16 == 0, "columns");
+  static constexpr int kSteps = (kCols + 31) / 32;
+  static constexpr int width(int st) { return kCols - 32 * st < 32 ? kCols - 32 * st : 32; }
 };
 
 // acc[a0 .. a0 + kC) += P * scale for one step of kC columns that starts at
-// column a0 of the warp's kHalf (tile column col0 + a0).  Block scales
+// column a0 of the warp's kCols (tile column col0 + a0).  Block scales
 // change only at 128-column boundaries, which fall on multiples of 16
 // columns of the warp's range; tile scales change per column.
 template <int kC, int a0, bool B_TILE>
@@ -202,17 +253,21 @@ __device__ __forceinline__ void tmem_ld_step(uint32_t taddr, uint32_t* r) {
     ptx::tmem_ld_32x32b_x16(taddr, r);
 }
 
-template <int BN, int CM, bool PROMOTE, bool OUT_BF16, bool B_TILE>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, bool OUT_BF16, bool B_TILE>
+__global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  using L = Cfg<BN, CM>;
+  using L = Cfg<BN, CM, PAIR, PW>;
+  constexpr int kPromoWarps = L::kPromoWarps;
   constexpr int STAGES = L::kStages;
   constexpr int TBUF = L::kTBuf;
-  constexpr int kHalf = BN / 2;         // columns per promotion warp
+  constexpr int kCols = L::kCols;  // columns per promotion warp
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kBM, BN);
-  constexpr uint32_t kStageTx = L::kABytes + L::kBBytes;  // bytes landing in this CTA
+  // a CTA pair runs M = 256 MMAs, each CTA holding 128 rows of A and of D
+  constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, BN);
+  // bytes one stage's full barrier waits for: what lands in this CTA, or,
+  // for a pair (whose leader's barrier counts both CTAs' copies), twice that
+  constexpr uint32_t kStageTx = (PAIR ? 2 : 1) * (L::kABytes + L::kBBytes);
   constexpr uint16_t kPeers = (1u << CM) - 1u;
 
   extern __shared__ uint8_t smem_raw[];
@@ -239,11 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
-      ptx::mbar_init(&empty[i], CM);  // one MMA commit from each CTA of the cluster
+      // one MMA commit from each CTA of the cluster (a pair has one issuer)
+      ptx::mbar_init(&empty[i], PAIR ? 1 : CM);
     }
     for (int i = 0; i < TBUF; ++i) {
       ptx::mbar_init(&tfull[i], 1);
-      ptx::mbar_init(&tempty[i], kPromoWarps);
+      // a pair's leader waits for both CTAs' promotion warps
+      ptx::mbar_init(&tempty[i], PAIR ? 2 * kPromoWarps : kPromoWarps);
     }
     for (int i = 0; i < kScaleSlots; ++i) {
       ptx::mbar_init(&sfull[i], 32);
@@ -254,8 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_base_slot, kTmemCols);
-    ptx::tmem_relinquish();
+    if (PAIR) {  // collective: both CTAs of the pair get the same columns
+      ptx::tmem_alloc_pair(tmem_base_slot, kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_base_slot, kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -272,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Warpgroup 0: producer, MMA issuer, scale loader (warp 3 idles).  Each
   // warpgroup changes its register allocation at the top of its own branch,
   // so that the code it runs is compiled against the new limit.
-  if constexpr (L::kRegSplit) ptx::regs_dec<kCtlRegs>();
+  if constexpr (L::kRegSplit) ptx::regs_dec<L::kCtlRegs>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -287,6 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
           if (!wait_bar(&empty[stage], phase ^ 1, abort_flag, kErrProducer)) { ok = false; break; }
           if ((int)it == p.skip_iter) continue;  // test hook: never arrives
+          if (PAIR) {
+            // both CTAs' copies complete on the leader's barrier
+            if (rank == 0) ptx::mbar_arrive_expect_tx(&full[stage], kStageTx);
+            const uint32_t fb = ptx::mapa(&full[stage], 0);
+            ptx::tma_load_2d_pair(sA + stage * L::kABytes, &tmap_a, fb, kb * kBK, mt * kBM);
+            ptx::tma_load_2d_pair(sB + stage * L::kBBytes, &tmap_b, fb, kb * kBK,
+                                  nt * BN + rank * L::kBH);
+            issued_mask |= 1u << stage;
+            continue;
+          }
           ptx::mbar_arrive_expect_tx(&full[stage], kStageTx);
           ptx::tma_load_2d(sA + stage * L::kABytes, &tmap_a, &full[stage], kb * kBK, mt * kBM);
           if (CM == 1)
@@ -298,8 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Drain: wait (bounded) until the last copy issued into each stage has
-      // landed, so no copy is in flight when the CTA exits.
-      const uint32_t last = it;
+      // landed, so no copy is in flight when the CTA exits.  A pair's
+      // follower has no full barriers of its own: its copies complete on the
+      // leader's, which the leader drains.
+      const uint32_t last = (PAIR && rank != 0) ? 0 : it;
       for (uint32_t s = 0; s < STAGES; ++s) {
         if (!(issued_mask & (1u << s)) || last == 0) continue;
         // the last iteration index < last that used stage s
@@ -314,7 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (for a CTA pair, the leader issues the pair's MMAs)
+    if (lane == 0 && (!PAIR || rank == 0)) {
       uint32_t it = 0, kt = 0;
       bool ok = true;
       for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
@@ -329,15 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
             const uint32_t d = tmem_base + buf * L::kTmemStride;
-#pragma unroll
-            for (int k = 0; k < kBK / 32; ++k)
-              ptx::mma_f8f6f4(d, ptx::smem_desc_k128_sw128(a0 + 32 * k),
-                              ptx::smem_desc_k128_sw128(b0 + 32 * k), kIdesc, k > 0);
-            if (CM == 1)
-              ptx::tc_commit(&empty[stage]);
+            issue_kgroup<PAIR>(d, a0, b0, kIdesc, false);
+            commit_stage<CM, PAIR>(&empty[stage], kPeers);
+            if (PAIR)
+              ptx::tc_commit_pair_mcast(&tfull[buf], kPeers);
             else
-              ptx::tc_commit_mcast(&empty[stage], kPeers);
-            ptx::tc_commit(&tfull[buf]);
+              ptx::tc_commit(&tfull[buf]);
           }
         } else {
           const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
@@ -350,23 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
-#pragma unroll
-            for (int k = 0; k < kBK / 32; ++k)
-              ptx::mma_f8f6f4(d, ptx::smem_desc_k128_sw128(a0 + 32 * k),
-                              ptx::smem_desc_k128_sw128(b0 + 32 * k), kIdesc,
-                              (kb > 0 || k > 0) ? 1u : 0u);
-            if (CM == 1)
-              ptx::tc_commit(&empty[stage]);
-            else
-              ptx::tc_commit_mcast(&empty[stage], kPeers);
+            issue_kgroup<PAIR>(d, a0, b0, kIdesc, kb > 0);
+            commit_stage<CM, PAIR>(&empty[stage], kPeers);
           }
           if (!ok) break;
-          ptx::tc_commit(&tfull[buf]);
+          if (PAIR)
+            ptx::tc_commit_pair_mcast(&tfull[buf], kPeers);
+          else
+            ptx::tc_commit(&tfull[buf]);
           ++kt;
         }
       }
       // Drain: every MMA this thread issued has completed before TMEM is freed.
-      ptx::tc_commit(drain);
+      if (PAIR)
+        ptx::tc_commit_pair(drain);
+      else
+        ptx::tc_commit(drain);
       const uint32_t addr = ptx::smem_addr(drain);
       const uint64_t t0 = ptx::globaltimer();
       while (!ptx::mbar_try_wait(addr, 0)) {
@@ -419,29 +490,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   } else {
     // ------------------------------------------------- promotion + epilogue
-    if constexpr (L::kRegSplit) ptx::regs_inc<kPromoRegs>();
+    if constexpr (L::kRegSplit) ptx::regs_inc<L::kPromoRegs>();
     const int w = warp - kFirstPromoWarp;
     const int lg = warp & 3;       // TMEM lane group this warp may access
-    const int ch = w >> 2;         // column half
+    const int ch = w >> 2;         // which kCols-wide column range
     const int row = lg * 32 + lane;
-    const int col0 = ch * kHalf;
+    const int col0 = ch * kCols;
     const uint32_t t_lane = (uint32_t)(lg * 32) << 16;
     uint32_t kt = 0, ks = 0;
     bool ok = true;
     for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
       const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
       const int m0 = mt * kBM, n0 = nt * BN;
-      float acc[kHalf];
+      float acc[kCols];
 #pragma unroll
-      for (int j = 0; j < kHalf; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
 
       if (PROMOTE) {
-        using PS = PromoSteps<kHalf>;
+        using PS = PromoSteps<kCols>;
         constexpr int kS = PS::kSteps;
         static_assert(kS <= 4, "steps");
         // Block scales: the first column of this warp's range that lies in
-        // the next 128-column block (kHalf when there is none).
-        const int a_split = B_TILE ? kHalf : ((n0 + col0) / 128 + 1) * 128 - (n0 + col0);
+        // the next 128-column block (kCols when there is none).
+        const int a_split = B_TILE ? kCols : ((n0 + col0) / 128 + 1) * 128 - (n0 + col0);
         const int nb_lo = (n0 + col0) / 128 - n0 / 128;
         for (int kb = 0; kb < KB; ++kb, ++kt, ++ks) {
           const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
@@ -454,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float f_lo = 0.0f, f_hi = 0.0f;
           if (!B_TILE) {
             f_lo = __fmul_rn(sa_r, scb[nb_lo]);
-            f_hi = a_split < kHalf ? __fmul_rn(sa_r, scb[nb_lo + 1]) : f_lo;
+            f_hi = a_split < kCols ? __fmul_rn(sa_r, scb[nb_lo + 1]) : f_lo;
           }
           bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
           if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
@@ -464,6 +535,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           // before step s's FMAs.  tcgen05.wait::ld waits for all of this
           // thread's loads, which is why only one step is ever in flight.
           const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
+          if constexpr (L::kLoadAll) {
+            // The whole partial of this warp in one round of loads; the
+            // buffer goes back to the MMA issuer before the FMAs.
+            uint32_t va[kCols];
+#pragma unroll
+            for (int c = 0; c < kCols; c += 16) ptx::tmem_ld_32x32b_x16(tcur + c, va + c);
+            ptx::tmem_ld_wait();
+            reg_fence<kCols>(va);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) release_tmem<PAIR>(&tempty[buf]);
+#pragma unroll
+            for (int c = 0; c < kCols; c += 16)
+              promote_step<16, 0, B_TILE>(acc + c, va + c, sa_r, scb, col0 + c, f_lo, f_hi,
+                                          a_split - c);
+          } else {
           uint32_t v[2][32];
           tmem_ld_step<PS::width(0)>(tcur, v[0]);
 #define FP8BS_STEP(S)                                                                     \
@@ -476,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       /* every TMEM read of this buffer is done: hand it back */                          \
       ptx::tc_fence_before();                                                             \
       __syncwarp();                                                                       \
-      if (lane == 0) ptx::mbar_arrive(&tempty[buf]);                                      \
+      if (lane == 0) release_tmem<PAIR>(&tempty[buf]);                                    \
     }                                                                                     \
     promote_step<PS::width(S), 32 * S, B_TILE>(acc, v[S & 1], sa_r, scb, col0, f_lo, f_hi, \
                                                a_split);                                  \
@@ -486,6 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           FP8BS_STEP(2)
           FP8BS_STEP(3)
 #undef FP8BS_STEP
+          }
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sempty[slot]);
         }
@@ -499,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sa_r = (m < p.M) ? __ldg(p.sa + m) : 0.0f;  // K-group 0
         const uint32_t tbase = tmem_base + t_lane + buf * L::kTmemStride + col0;
 #pragma unroll
-        for (int c0 = 0; c0 < kHalf / 16; ++c0) {
+        for (int c0 = 0; c0 < kCols / 16; ++c0) {
           uint32_t v[16];
           ptx::tmem_ld_32x32b_x16(tbase + c0 * 16, v);
           ptx::tmem_ld_wait();
@@ -514,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+        if (lane == 0) release_tmem<PAIR>(&tempty[buf]);
         ++kt;
       }
       if (!ok) break;
@@ -525,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (OUT_BF16) {
           __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.c) + (size_t)m * p.N;
 #pragma unroll
-          for (int j = 0; j < kHalf; j += 8) {
+          for (int j = 0; j < kCols; j += 8) {
             const int n = n0 + col0 + j;
             if (n < p.N) {
               uint4 o;
@@ -543,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           float* crow = static_cast<float*>(p.c) + (size_t)m * p.N;
 #pragma unroll
-          for (int j = 0; j < kHalf; j += 4) {
+          for (int j = 0; j < kCols; j += 4) {
             const int n = n0 + col0 + j;
             if (n < p.N)
               *reinterpret_cast<float4*>(crow + n) =
@@ -557,20 +645,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown: all roles done (or aborted); free TMEM
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, kTmemCols);
-  }
   if (CM > 1) {
-    // After an abort a peer's multicast may still be landing in this CTA's
+    // After an abort a peer's copy may still be landing in this CTA's
     // shared memory: give it time before leaving (normal runs skip this).
     if (*abort_flag) {
       const uint64_t t0 = ptx::globaltimer();
       while (ptx::globaltimer() - t0 < 1000000ull) {
       }
     }
-    // neither CTA leaves while the other may still write into it
+    // neither CTA leaves (or frees TMEM the pair's MMAs write) while the
+    // other may still write into it
     ptx::cluster_sync();
+  }
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    if (PAIR)
+      ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -601,10 +693,11 @@ struct KernelInfo {
   int max_ctas = 0;  // persistent grid size (a multiple of CM)
 };
 
-template <int BN, int CM, bool PROMOTE, bool OUT_BF16, bool B_TILE>
+template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, bool OUT_BF16, bool B_TILE>
 cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
-  using L = Cfg<BN, CM>;
-  auto kern = gemm_kernel<BN, CM, PROMOTE, OUT_BF16, B_TILE>;
+  using L = Cfg<BN, CM, PAIR, PW>;
+  constexpr int kThreads = L::kThreads;
+  auto kern = gemm_kernel<BN, CM, PAIR, PW, PROMOTE, OUT_BF16, B_TILE>;
   static KernelInfo info[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -618,7 +711,7 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
       e = cudaFuncGetAttributes(&fa, kern);
       // setmaxnreg.inc waits until the registers it asks for are free: a
       // split larger than the launch's allocation would never proceed.
-      if (e == cudaSuccess && fa.numRegs * kThreads < kSplitRegsNeeded)
+      if (e == cudaSuccess && fa.numRegs * kThreads < L::kSplitRegsNeeded)
         e = cudaErrorInvalidConfiguration;
     }
     int ctas = num_sms_current_device();
@@ -693,6 +786,11 @@ enum TileShape {
   kTile128x128x2 = 3,
   kTile128x160x2 = 4,
   kTile128x192x2 = 5,
+  kTile256x256Pair = 6,
+  kTile256x224Pair = 7,
+  kTile256x192Pair = 8,
+  kTile128x192x2W12 = 9,
+  kTile256x192PairW12 = 10,
 };
 
 TileShape choose_tile(int64_t M, int64_t N, int sms) {
@@ -725,18 +823,28 @@ cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
   int shape = g.tile;
   if (shape < 0) shape = choose_tile(g.M, g.N, num_sms_current_device());
   switch (shape) {
+    case kTile128x192x2W12:
+      return launch_variant<192, 2, false, 12, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile256x192PairW12:
+      return launch_variant<192, 2, true, 12, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile256x256Pair:
+      return launch_variant<256, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile256x224Pair:
+      return launch_variant<224, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile256x192Pair:
+      return launch_variant<192, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile128x256x2:
-      return launch_variant<256, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<256, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile128x224x2:
-      return launch_variant<224, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<224, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile128x192x2:
-      return launch_variant<192, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<192, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile128x160x2:
-      return launch_variant<160, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<160, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile128x128x2:
-      return launch_variant<128, 2, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<128, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     default:
-      return launch_variant<128, 1, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<128, 1, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
   }
 }
 

@@ -68,7 +68,7 @@ __device__ __forceinline__ float fmax_abs_nan(float acc, float x) {
 }
 
 struct GroupScale {
-  float s, r;
+  float s, nr;  // scale, and -fl32(1 / s) on the fast path
   bool fast;
 };
 
@@ -79,41 +79,46 @@ __device__ __forceinline__ GroupScale make_scale(uint32_t mag_no_nan_bits, bool 
   GroupScale g;
   g.s = group_scale(__uint_as_float(bf16 ? mag_no_nan_bits << 16 : mag_no_nan_bits));
   g.fast = !special && g.s >= kFastScaleMin;
-  g.r = g.fast ? __frcp_rn(g.s) : 0.0f;
+  g.nr = g.fast ? -__frcp_rn(g.s) : 0.0f;
   return g;
 }
 
-// Two bf16 (one word, element 0 in the low half) -> two codes.
-__device__ __forceinline__ uint32_t codes_bf16x2(uint32_t w, const GroupScale& g) {
-  const float2 x = make_float2(bf16_lo(w), bf16_hi(w));
+// Four bf16 (two words, element 0 in the low half of wa) -> four codes,
+// element 0 in byte 0.  The fast path converts the negated quotients and
+// flips the four sign bits at once.
+__device__ __forceinline__ uint32_t codes_bf16x4(uint32_t wa, uint32_t wb, const GroupScale& g) {
+  const float2 xa = make_float2(bf16_lo(wa), bf16_hi(wa));
+  const float2 xb = make_float2(bf16_lo(wb), bf16_hi(wb));
   if (g.fast) {
-    const float2 q = quotient_1step_x2(x, g.s, g.r);
-    return e4m3x2(q.x, q.y);
+    const float2 qa = neg_quotient_1step_x2(xa, g.s, g.nr);
+    const float2 qb = neg_quotient_1step_x2(xb, g.s, g.nr);
+    return (e4m3x2(qa.x, qa.y) | (e4m3x2(qb.x, qb.y) << 16)) ^ 0x80808080u;
   }
-  return e4m3x2_nan(quotient_general(x.x, g.s), quotient_general(x.y, g.s));
+  return e4m3x2_nan(quotient_general(xa.x, g.s), quotient_general(xa.y, g.s)) |
+         (e4m3x2_nan(quotient_general(xb.x, g.s), quotient_general(xb.y, g.s)) << 16);
 }
 
 // Eight bf16 (one 16-byte vector) -> eight codes in two words.
 __device__ __forceinline__ uint2 codes_bf16x8(uint4 v, const GroupScale& g) {
-  uint2 o;
-  o.x = codes_bf16x2(v.x, g) | (codes_bf16x2(v.y, g) << 16);
-  o.y = codes_bf16x2(v.z, g) | (codes_bf16x2(v.w, g) << 16);
-  return o;
+  return make_uint2(codes_bf16x4(v.x, v.y, g), codes_bf16x4(v.z, v.w, g));
 }
 
-// Two FP32 values (full 24-bit significands) -> two codes.
-__device__ __forceinline__ uint32_t codes_f32x2(float a, float b, const GroupScale& g) {
+// Four FP32 values (full 24-bit significands) -> four codes.
+__device__ __forceinline__ uint32_t codes_f32x4(float a, float b, float c, float d,
+                                                const GroupScale& g) {
   if (g.fast) {
-    const float2 q = quotient_2step_x2(make_float2(a, b), g.s, g.r);
-    return e4m3x2(q.x, q.y);
+    const float2 q0 = neg_quotient_2step_x2(make_float2(a, b), g.s, g.nr);
+    const float2 q1 = neg_quotient_2step_x2(make_float2(c, d), g.s, g.nr);
+    return (e4m3x2(q0.x, q0.y) | (e4m3x2(q1.x, q1.y) << 16)) ^ 0x80808080u;
   }
-  return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s));
+  return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s)) |
+         (e4m3x2_nan(quotient_general(c, g.s), quotient_general(d, g.s)) << 16);
 }
 
 __device__ __forceinline__ GroupScale shfl_scale(const GroupScale& g, int src) {
   GroupScale o;
   o.s = __shfl_sync(kFull, g.s, src);
-  o.r = __shfl_sync(kFull, g.r, src);
+  o.nr = __shfl_sync(kFull, g.nr, src);
   o.fast = __shfl_sync(kFull, (int)g.fast, src) != 0;
   return o;
 }
@@ -496,19 +501,14 @@ __global__ void __launch_bounds__(256) quant_act_128x1_kernel(
   const GroupScale ghi = make_scale(mn >> 16, (mp >> 16) >= kBf16Inf, true);
   uint32_t olo[8], ohi[8];
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
+  for (int i = 0; i < 32; i += 4) {
     const uint32_t w0 = tw[(part * 32 + i) * 64 + cp];
     const uint32_t w1 = tw[(part * 32 + i + 1) * 64 + cp];
-    // (row i, row i + 1) of each column
-    const uint32_t clo = codes_bf16x2(__byte_perm(w0, w1, 0x5410), glo);
-    const uint32_t chi = codes_bf16x2(__byte_perm(w0, w1, 0x7632), ghi);
-    if ((i & 2) == 0) {
-      olo[i >> 2] = clo;
-      ohi[i >> 2] = chi;
-    } else {
-      olo[i >> 2] |= clo << 16;
-      ohi[i >> 2] |= chi << 16;
-    }
+    const uint32_t w2 = tw[(part * 32 + i + 2) * 64 + cp];
+    const uint32_t w3 = tw[(part * 32 + i + 3) * 64 + cp];
+    // rows i .. i + 3 of each column
+    olo[i >> 2] = codes_bf16x4(__byte_perm(w0, w1, 0x5410), __byte_perm(w2, w3, 0x5410), glo);
+    ohi[i >> 2] = codes_bf16x4(__byte_perm(w0, w1, 0x7632), __byte_perm(w2, w3, 0x7632), ghi);
   }
   uint4* dlo = reinterpret_cast<uint4*>(qT + (k0 + 2 * cp) * M + m0 + part * 32);
   uint4* dhi = reinterpret_cast<uint4*>(qT + (k0 + 2 * cp + 1) * M + m0 + part * 32);
@@ -586,19 +586,15 @@ __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
   }
   uint32_t o[4][4];
 #pragma unroll
-  for (int i = 0; i < 16; i += 2) {
+  for (int i = 0; i < 16; i += 4) {
     const int r = part * 16 + i;
-    float x0[4], x1[4];
+    float x0[4], x1[4], x2[4], x3[4];
     dequant4(tw[r * 32 + cq], srow[r], x0);
     dequant4(tw[(r + 1) * 32 + cq], srow[r + 1], x1);
+    dequant4(tw[(r + 2) * 32 + cq], srow[r + 2], x2);
+    dequant4(tw[(r + 3) * 32 + cq], srow[r + 3], x3);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t code = codes_f32x2(x0[c], x1[c], g[c]);
-      if ((i & 2) == 0)
-        o[c][i >> 2] = code;
-      else
-        o[c][i >> 2] |= code << 16;
-    }
+    for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c)

@@ -160,7 +160,12 @@ fp8bs_status fp8bs_gemm_ex(const uint8_t *a, const float *sa,
  * device's SMs, weighted by each shape's efficiency.
  *   128x128            one CTA per tile;
  *   128xBN_CLUSTER2    clusters of two CTAs on vertically adjacent tiles
- *                      that share (and multicast) the B tile.
+ *                      that share (and multicast) the B tile;
+ *   256xBN_PAIR        a CTA pair whose tensor cores compute one 256xBN
+ *                      tile together, each CTA holding half of A and half
+ *                      of B;
+ *   ..._W12            the same with 12 promotion warps of 64 columns each
+ *                      (8 otherwise).
  */
 typedef enum {
   FP8BS_TILE_AUTO = -1,
@@ -169,7 +174,12 @@ typedef enum {
   FP8BS_TILE_128x256_CLUSTER2 = 2,
   FP8BS_TILE_128x128_CLUSTER2 = 3,
   FP8BS_TILE_128x160_CLUSTER2 = 4,
-  FP8BS_TILE_128x192_CLUSTER2 = 5
+  FP8BS_TILE_128x192_CLUSTER2 = 5,
+  FP8BS_TILE_256x256_PAIR = 6,
+  FP8BS_TILE_256x224_PAIR = 7,
+  FP8BS_TILE_256x192_PAIR = 8,
+  FP8BS_TILE_128x192_CLUSTER2_W12 = 9,
+  FP8BS_TILE_256x192_PAIR_W12 = 10
 } fp8bs_tile_shape;
 
 /*

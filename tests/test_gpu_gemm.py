@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 BLOCK, TILE = 0, 1
 # every output-tile shape of the kernel (the automatic choice differs by shape)
-TILES = [0, 1, 2, 3, 4, 5]
+TILES = list(range(11))
 
 
 def _quantized_pair(oracle_mod, M, N, K, seed, bkind):
@@ -22,7 +22,13 @@ def _quantized_pair(oracle_mod, M, N, K, seed, bkind):
     a_bits, _ = synth.normal_with_outlier_columns(rng, (M, K), 3, 50.0)
     a, sa = oracle_mod.quant_act_1x128(a_bits)
     if bkind == BLOCK:
-        b, sb = oracle_mod.quant_weight_128x128(synth.normal(rng, (N, K), 0.02))
+        # block scales cover ceil(N / 128) row blocks: quantize the weight
+        # padded with zero rows to whole blocks, keep its first N code rows
+        nb = (N + 127) // 128
+        w = np.zeros((nb * 128, K), np.uint16)
+        w[:N] = synth.normal(rng, (N, K), 0.02)
+        b, sb = oracle_mod.quant_weight_128x128(w)
+        b = np.ascontiguousarray(b[:N])
     else:
         b, sb = oracle_mod.quant_act_1x128(synth.normal(rng, (N, K), 1e-3))
     return a, sa, b, sb
