@@ -24,7 +24,8 @@ TILE_AUTO, TILE_128x128, TILE_128x224_CLUSTER2, TILE_128x256_CLUSTER2 = -1, 0, 1
 TILE_128x128_CLUSTER2, TILE_128x160_CLUSTER2, TILE_128x192_CLUSTER2 = 3, 4, 5
 TILE_256x256_PAIR, TILE_256x224_PAIR, TILE_256x192_PAIR = 6, 7, 8
 TILE_128x192_CLUSTER2_W12, TILE_256x192_PAIR_W12 = 9, 10
-TILES = tuple(range(11))
+TILE_256x128_PAIR, TILE_256x160_PAIR = 11, 12
+TILES = tuple(range(13))
 BSCALE_BLOCK_128x128, BSCALE_TILE_1x128 = 0, 1
 GROUP = 128
 

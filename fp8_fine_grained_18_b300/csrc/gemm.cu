@@ -791,6 +791,8 @@ enum TileShape {
   kTile256x192Pair = 8,
   kTile128x192x2W12 = 9,
   kTile256x192PairW12 = 10,
+  kTile256x128Pair = 11,
+  kTile256x160Pair = 12,
 };
 
 TileShape choose_tile(int64_t M, int64_t N, int sms) {
@@ -827,6 +829,10 @@ cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
       return launch_variant<192, 2, false, 12, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile256x192PairW12:
       return launch_variant<192, 2, true, 12, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile256x128Pair:
+      return launch_variant<128, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+    case kTile256x160Pair:
+      return launch_variant<160, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile256x256Pair:
       return launch_variant<256, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
     case kTile256x224Pair:

@@ -179,7 +179,9 @@ typedef enum {
   FP8BS_TILE_256x224_PAIR = 7,
   FP8BS_TILE_256x192_PAIR = 8,
   FP8BS_TILE_128x192_CLUSTER2_W12 = 9,
-  FP8BS_TILE_256x192_PAIR_W12 = 10
+  FP8BS_TILE_256x192_PAIR_W12 = 10,
+  FP8BS_TILE_256x128_PAIR = 11,
+  FP8BS_TILE_256x160_PAIR = 12
 } fp8bs_tile_shape;
 
 /*

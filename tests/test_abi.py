@@ -87,7 +87,7 @@ def test_gemm_argument_errors(libfp8bs):
     assert L.fp8bs_debug_gemm_stall(FAKE, FAKE, FAKE, FAKE, 8, 256, 128, FAKE, -1, -1, None) == m.ERR_INVALID_ARG
     targs = lambda tile: (FAKE, FAKE, FAKE, FAKE, 0, 8, 256, 128, FAKE, 0, 1, tile, None)  # noqa: E731
     assert L.fp8bs_gemm_tiled(*targs(-2)) == m.ERR_INVALID_ARG
-    assert L.fp8bs_gemm_tiled(*targs(11)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_tiled(*targs(13)) == m.ERR_INVALID_ARG
     assert L.fp8bs_gemm_tiled(FAKE, FAKE, FAKE, FAKE, 0, 8, 256, 100, FAKE, 0, 1, 2, None) == \
         m.ERR_UNSUPPORTED_SHAPE
 
