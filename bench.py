@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on (sha of gemm.cu, ptx.cuh,
 # fp8_common.cuh); reported as null once the source has changed.
-TRAFFIC = {"gemm": {"bytes": 86836224 + 35640320, "src_sha": "8834caca0720c9e9"}}
+TRAFFIC = {"gemm": {"bytes": 86919424 + 35751168, "src_sha": "a985ce3c1daf6a2c"}}
 
 
 def kernel_source_sha():
@@ -193,6 +193,10 @@ def algorithmic_bytes_q1(M, K):
 
 def algorithmic_bytes_q2(N, K, transposed=False):
     return N * K * (4 if transposed else 3) + 4 * (N // 128) * (K // 128) * (2 if transposed else 1)
+
+
+def algorithmic_bytes_dual(M, K):
+    return M * K * 4 + 2 * 4 * M * (K // 128)
 
 
 def algorithmic_bytes_q3(M, K):
@@ -459,7 +463,24 @@ def measure_rows(fp8bs, torch, dev, peaks):
     quant_row("Q1 moe A 8192x7168", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
               algorithmic_bytes_q1(8192, 7168))
     gemm_row("G1 moe 8192x4096x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
-    del a, b, qa, sa, qb, sb
+    # the GEMM output quantized for the next layer: fused epilogue against
+    # the BF16 output written to HBM and quantized by Q1 afterwards
+    c8, cs8 = fp8bs.gemm_quant_out(qa, sa, qb, sb, 0)
+    ms_f = _time_ms(lambda: fp8bs.gemm_quant_out(qa, sa, qb, sb, 0, out=c8, out_scales=cs8),
+                    torch, flush=flush)
+    cbf = torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev)
+    qc, sc = fp8bs.quant_act_1x128(cbf)
+
+    def unfused():
+        fp8bs.gemm(qa, sa, qb, sb, 0, out_dtype=torch.bfloat16, out=cbf)
+        fp8bs.quant_act_1x128(cbf, q=qc, scales=sc)
+    ms_u = _time_ms(unfused, torch, flush=flush)
+    tflop = 2.0 * 8192 * 4096 * 7168 / 1e12
+    rows["G1+Q moe 8192x4096x7168, output quantized 1x128 in the epilogue"] = {
+        "ms": round(ms_f, 4), "TFLOP/s": round(tflop / (ms_f * 1e-3), 1),
+        "frac_fp8_peak": round(tflop / (ms_f * 1e-3) / fp8_peak, 4),
+        "unfused_gemm_bf16_then_Q1_ms": round(ms_u, 4)}
+    del a, b, qa, sa, qb, sb, c8, cs8, cbf, qc, sc
 
     # backward chain
     bwd = synth.make_inputs("bwd")
@@ -473,6 +494,10 @@ def measure_rows(fp8bs, torch, dev, peaks):
               lambda: fp8bs.quant_act_1x128(dy, transpose_out=True, q=qdyT, scales=sdyT),
               algorithmic_bytes_q1(4096, 7168))
     qdy, sdy = fp8bs.quant_act_1x128(dy)
+    bufs = fp8bs.quant_act_dual(dy)
+    quant_row("Q1+Q1T fused dY 4096x7168 (both tilings, one read)",
+              lambda: fp8bs.quant_act_dual(dy, *bufs), algorithmic_bytes_dual(4096, 7168))
+    del bufs
     qw, sw, qwT, swT = fp8bs.quant_weight_128x128(wt, transposed=True)
     quant_row("Q2+T W 7168x2048 (with transposed copy)",
               lambda: fp8bs.quant_weight_128x128(wt, transposed=True, q=qw, scales=sw, qT=qwT, scalesT=swT),

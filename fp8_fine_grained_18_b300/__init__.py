@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
-OUT_BF16, OUT_F32 = 0, 1
+OUT_BF16, OUT_F32, OUT_E4M3_1x128 = 0, 1, 2
 TILE_AUTO, TILE_128x128, TILE_128x224_CLUSTER2, TILE_128x256_CLUSTER2 = -1, 0, 1, 2
 TILE_128x128_CLUSTER2, TILE_128x160_CLUSTER2, TILE_128x192_CLUSTER2 = 3, 4, 5
 TILE_256x256_PAIR, TILE_256x224_PAIR, TILE_256x192_PAIR = 6, 7, 8
@@ -39,10 +39,13 @@ _P, _I64, _I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
 _SIGS = {
     "fp8bs_quant_act_1x128": [_P, _I64, _I64, _I, _P, _P, _P],
     "fp8bs_quant_weight_128x128": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "fp8bs_quant_act_dual": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "fp8bs_quant_per_tensor": [_P, _I64, _I64, _P, _P, _P, _I64, _P],
     "fp8bs_requant_1x128_to_128x1": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8bs_gemm": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P],
     "fp8bs_gemm_ex": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _P],
     "fp8bs_gemm_tiled": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _I, _P],
+    "fp8bs_gemm_quant_out": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P],
     "fp8bs_debug_gemm_stall": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I, _I, _P],
     "fp8bs_get_device_error": [_P],
     "fp8bs_status_string": [_I],
@@ -106,6 +109,20 @@ def quant_act_1x128(x: torch.Tensor, transpose_out: bool = False, q=None, scales
     return q, scales
 
 
+def quant_act_dual(x: torch.Tensor, q=None, scales=None, qT=None, scalesT=None):
+    """bf16 x[M, K] -> (codes [M, K], scales [K/128, M], codesT [K, M],
+    scalesT [M/128, K]): both tilings of quant_act_1x128 from one read."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    M, K = x.shape
+    q = _empty((M, K), torch.uint8, x) if q is None else q
+    scales = _empty((K // GROUP, M), torch.float32, x) if scales is None else scales
+    qT = _empty((K, M), torch.uint8, x) if qT is None else qT
+    scalesT = _empty((M // GROUP, K), torch.float32, x) if scalesT is None else scalesT
+    _check(_lib.fp8bs_quant_act_dual(_ptr(x), M, K, _ptr(q), _ptr(scales), _ptr(qT),
+                                     _ptr(scalesT), _stream(x)), "fp8bs_quant_act_dual")
+    return q, scales, qT, scalesT
+
+
 def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, q=None, scales=None,
                          qT=None, scalesT=None):
     """bf16 w[N, K] -> (codes [N, K], scales [N/128, K/128]) and, with
@@ -122,6 +139,22 @@ def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, q=None, scal
                                            _ptr(scalesT if transposed else None), _stream(w)),
            "fp8bs_quant_weight_128x128")
     return (q, scales, qT, scalesT) if transposed else (q, scales)
+
+
+def quant_per_tensor(x: torch.Tensor, q=None, scale=None, bcast_shape=None, bcast=None):
+    """Per-tensor baseline: x bf16 [rows, cols] -> (q uint8, scale float32 [1],
+    bcast float32 of bcast_shape filled with the scale, or None)."""
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    rows, cols = x.shape
+    q = _empty((rows, cols), torch.uint8, x) if q is None else q
+    scale = _empty((1,), torch.float32, x) if scale is None else scale
+    if bcast is None and bcast_shape is not None:
+        bcast = _empty(tuple(bcast_shape), torch.float32, x)
+    nb = 0 if bcast is None else bcast.numel()
+    _check(_lib.fp8bs_quant_per_tensor(_ptr(x), rows, cols, _ptr(q), _ptr(scale),
+                                       _ptr(bcast) if bcast is not None else None, nb,
+                                       _stream(x)), "fp8bs_quant_per_tensor")
+    return q, scale, bcast
 
 
 def requant_1x128_to_128x1(q: torch.Tensor, scales: torch.Tensor, qT=None, scalesT=None):
@@ -150,6 +183,21 @@ def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
                                  _ptr(c), odt, int(bool(promote)), int(tile), _stream(a)),
            "fp8bs_gemm")
     return c
+
+
+def gemm_quant_out(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
+                   bkind: int = BSCALE_BLOCK_128x128, out=None, out_scales=None):
+    """The promoted GEMM with its FP32 result quantized 1x128 in the epilogue.
+
+    Returns (c uint8 [M, N] E4M3 codes, c_scales float32 [N/128, M])."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8
+    M, K = a.shape
+    N = b.shape[0]
+    c = _empty((M, N), torch.uint8, a) if out is None else out
+    cs = _empty((N // GROUP, M), torch.float32, a) if out_scales is None else out_scales
+    _check(_lib.fp8bs_gemm_quant_out(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K,
+                                     _ptr(c), _ptr(cs), _stream(a)), "fp8bs_gemm_quant_out")
+    return c, cs
 
 
 def debug_gemm_stall(a, sa, b, sb, skip_iter: int, out=None, tile: int = TILE_AUTO):

@@ -13,6 +13,7 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 fp8bs_status cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return FP8BS_OK;
@@ -50,18 +51,22 @@ constexpr int64_t kMaxDim = (int64_t)1 << 31;  // kernels index rows with int32
 fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
                          fp8bs_out_dtype out, int promote, int skip_iter, int tile,
-                         fp8bs_stream_t stream) {
+                         fp8bs_stream_t stream, float* c_scales = nullptr) {
   if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
   if (bkind != FP8BS_BSCALE_BLOCK_128x128 && bkind != FP8BS_BSCALE_TILE_1x128)
     return FP8BS_ERR_INVALID_ARG;
-  if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+  if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32 && out != FP8BS_OUT_E4M3_1x128)
+    return FP8BS_ERR_INVALID_ARG;
+  if (out == FP8BS_OUT_E4M3_1x128 && (promote != 1 || !c_scales)) return FP8BS_ERR_INVALID_ARG;
   if (promote != 0 && promote != 1) return FP8BS_ERR_INVALID_ARG;
   if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_256x160_PAIR) return FP8BS_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FP8BS_OK;
   if (!a || !sa || !b || !sb || !c) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (out == FP8BS_OUT_E4M3_1x128 && N % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(c))
+  if (!aligned16(a) || !aligned16(sa) || !aligned16(b) || !aligned16(sb) || !aligned16(c) ||
+      (c_scales && !aligned16(c_scales)))
     return FP8BS_ERR_MISALIGNED;
   fp8bs_status st = check_device();
   if (st != FP8BS_OK) return st;
@@ -75,7 +80,8 @@ fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, co
   g.N = N;
   g.K = K;
   g.c = c;
-  g.out_bf16 = out == FP8BS_OUT_BF16;
+  g.c_scales = c_scales;
+  g.out = out == FP8BS_OUT_BF16 ? 1 : out == FP8BS_OUT_E4M3_1x128 ? 2 : 0;
   g.promote = promote != 0;
   g.skip_iter = skip_iter;
   g.tile = tile;
@@ -103,6 +109,23 @@ fp8bs_status fp8bs_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, int
   return cuda_status(e);
 }
 
+fp8bs_status fp8bs_quant_act_dual(const void* x_bf16, int64_t M, int64_t K, uint8_t* q,
+                                  float* scales, uint8_t* qT, float* scalesT,
+                                  fp8bs_stream_t stream) {
+  if (M < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (!x_bf16 || !q || !scales || !qT || !scalesT) return FP8BS_ERR_INVALID_ARG;
+  if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (K / 128 > 65535 || M / 128 > 65535) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales) || !aligned16(qT) ||
+      !aligned16(scalesT))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(
+      fp8bs::launch_quant_act_dual(x_bf16, M, K, q, scales, qT, scalesT, as_cuda(stream)));
+}
+
 fp8bs_status fp8bs_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K, uint8_t* q,
                                         float* scales, uint8_t* qT, float* scalesT,
                                         fp8bs_stream_t stream) {
@@ -119,6 +142,25 @@ fp8bs_status fp8bs_quant_weight_128x128(const void* w_bf16, int64_t N, int64_t K
   if (st != FP8BS_OK) return st;
   return cuda_status(
       fp8bs::launch_quant_weight_128x128(w_bf16, N, K, q, scales, qT, scalesT, as_cuda(stream)));
+}
+
+fp8bs_status fp8bs_quant_per_tensor(const void* x_bf16, int64_t rows, int64_t cols, uint8_t* q,
+                                    float* scale, float* scales_bcast, int64_t n_bcast,
+                                    fp8bs_stream_t stream) {
+  if (rows < 0 || cols < 0 || n_bcast < 0) return FP8BS_ERR_INVALID_ARG;
+  if (n_bcast > 0 && !scales_bcast) return FP8BS_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return FP8BS_OK;
+  if (!x_bf16 || !q || !scale) return FP8BS_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || rows >= kMaxDim * 64 || cols >= kMaxDim * 64 ||
+      rows > ((int64_t)1 << 40) / cols || n_bcast > ((int64_t)1 << 40))
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(q) || !aligned4(scale) ||
+      (scales_bcast && !aligned4(scales_bcast)))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(fp8bs::launch_quant_per_tensor(x_bf16, rows * cols, q, scale, scales_bcast,
+                                                    n_bcast, as_cuda(stream)));
 }
 
 fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t* q, const float* scales, int64_t M,
@@ -155,6 +197,14 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t* a, const float* sa, const uint8_t* 
                               int64_t K, void* c, fp8bs_out_dtype out, int promote,
                               fp8bs_tile_shape tile, fp8bs_stream_t stream) {
   return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, promote, -1, tile, stream);
+}
+
+fp8bs_status fp8bs_gemm_quant_out(const uint8_t* a, const float* sa, const uint8_t* b,
+                                   const float* sb, fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                                   int64_t K, uint8_t* c, float* c_scales,
+                                   fp8bs_stream_t stream) {
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, FP8BS_OUT_E4M3_1x128, 1, -1,
+                     FP8BS_TILE_AUTO, stream, c_scales);
 }
 
 fp8bs_status fp8bs_debug_gemm_stall(const uint8_t* a, const float* sa, const uint8_t* b,

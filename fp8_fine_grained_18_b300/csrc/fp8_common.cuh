@@ -96,4 +96,39 @@ __device__ __forceinline__ uint32_t e4m3x2_nan(float lo, float hi) {
   return c;
 }
 
+// Max of |x| that propagates NaN (a NaN in the group shows up as NaN).
+__device__ __forceinline__ float fmax_abs_nan(float acc, float x) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(acc), "f"(fabsf(x)));
+  return r;
+}
+
+struct GroupScale {
+  float s, nr;  // scale, and -fl32(1 / s) on the fast path
+  bool fast;
+};
+
+// Scale of a group from its amax given as a bit pattern (bf16 when bf16 is
+// true, else FP32); special = the group holds Inf or NaN.
+__device__ __forceinline__ GroupScale make_scale(uint32_t mag_no_nan_bits, bool special,
+                                                 bool bf16) {
+  GroupScale g;
+  g.s = group_scale(__uint_as_float(bf16 ? mag_no_nan_bits << 16 : mag_no_nan_bits));
+  g.fast = !special && g.s >= kFastScaleMin;
+  g.nr = g.fast ? -__frcp_rn(g.s) : 0.0f;
+  return g;
+}
+
+// Four FP32 values (full 24-bit significands) -> four codes.
+__device__ __forceinline__ uint32_t codes_f32x4(float a, float b, float c, float d,
+                                                const GroupScale& g) {
+  if (g.fast) {
+    const float2 q0 = neg_quotient_2step_x2(make_float2(a, b), g.s, g.nr);
+    const float2 q1 = neg_quotient_2step_x2(make_float2(c, d), g.s, g.nr);
+    return (e4m3x2(q0.x, q0.y) | (e4m3x2(q1.x, q1.y) << 16)) ^ 0x80808080u;
+  }
+  return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s)) |
+         (e4m3x2_nan(quotient_general(c, g.s), quotient_general(d, g.s)) << 16);
+}
+
 }  // namespace fp8bs

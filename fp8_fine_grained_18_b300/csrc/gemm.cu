@@ -69,6 +69,7 @@ struct Params {
   const float* sa;
   const float* sb;
   void* c;
+  float* c_scales;  // E4M3 output: [N/128][M]
   int M, N, K, KB;
   int num_m_units, num_units;  // a unit = CM vertically adjacent 128 x BN tiles
   int skip_iter;
@@ -253,7 +254,12 @@ __device__ __forceinline__ void tmem_ld_step(uint32_t taddr, uint32_t* r) {
     ptx::tmem_ld_32x32b_x16(taddr, r);
 }
 
-template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, bool OUT_BF16, bool B_TILE>
+// Output kinds: FP32, BF16 (round to nearest even), or E4M3 codes with one
+// FP32 scale per 1x128 tile of each output row (the next layer's activation
+// quantized in the epilogue).
+enum : int { kOutF32 = 0, kOutBf16 = 1, kOutE4m3 = 2 };
+
+template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
 __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const Params p) {
@@ -610,7 +616,38 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       // ---- epilogue: registers -> global (bf16 RNE or fp32)
       const int m = m0 + row;
       if (m < p.M) {
-        if (OUT_BF16) {
+        if constexpr (OUT == kOutE4m3) {
+          // One 1x128 group of the output row per thread: the warp's
+          // kCols = 128 columns start on a multiple of 128.  Same rule as the
+          // activation quantizer on FP32 values: s = fl32(amax / 448), codes
+          // of fl32(x / s) (two correction steps: x is a full FP32 value).
+          static_assert(kCols == 128, "one 1x128 group per promotion thread");
+          const int n = n0 + col0;
+          if (n < p.N) {
+            float amax = 0.0f;  // NaN if the group holds a NaN
+#pragma unroll
+            for (int j2 = 0; j2 < kCols; ++j2) amax = fmax_abs_nan(amax, acc[j2]);
+            float mn = amax;
+            if (amax != amax) {  // rare: recount ignoring NaN
+              mn = 0.0f;
+#pragma unroll
+              for (int j2 = 0; j2 < kCols; ++j2) mn = fmaxf(mn, fabsf(acc[j2]));
+            }
+            const GroupScale g =
+                make_scale(__float_as_uint(mn), !(amax < __uint_as_float(0x7F800000u)), false);
+            uint8_t* crow = static_cast<uint8_t*>(p.c) + (size_t)m * p.N + n;
+#pragma unroll
+            for (int j2 = 0; j2 < kCols; j2 += 16) {
+              uint4 o;
+              o.x = codes_f32x4(acc[j2], acc[j2 + 1], acc[j2 + 2], acc[j2 + 3], g);
+              o.y = codes_f32x4(acc[j2 + 4], acc[j2 + 5], acc[j2 + 6], acc[j2 + 7], g);
+              o.z = codes_f32x4(acc[j2 + 8], acc[j2 + 9], acc[j2 + 10], acc[j2 + 11], g);
+              o.w = codes_f32x4(acc[j2 + 12], acc[j2 + 13], acc[j2 + 14], acc[j2 + 15], g);
+              *reinterpret_cast<uint4*>(crow + j2) = o;
+            }
+            p.c_scales[(size_t)(n / 128) * p.M + m] = g.s;
+          }
+        } else if (OUT == kOutBf16) {
           __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.c) + (size_t)m * p.N;
 #pragma unroll
           for (int j = 0; j < kCols; j += 8) {
@@ -693,11 +730,11 @@ struct KernelInfo {
   int max_ctas = 0;  // persistent grid size (a multiple of CM)
 };
 
-template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, bool OUT_BF16, bool B_TILE>
+template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
 cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   using L = Cfg<BN, CM, PAIR, PW>;
   constexpr int kThreads = L::kThreads;
-  auto kern = gemm_kernel<BN, CM, PAIR, PW, PROMOTE, OUT_BF16, B_TILE>;
+  auto kern = gemm_kernel<BN, CM, PAIR, PW, PROMOTE, OUT, B_TILE>;
   static KernelInfo info[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -745,6 +782,7 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   p.sa = g.sa;
   p.sb = g.sb;
   p.c = g.c;
+  p.c_scales = g.c_scales;
   p.M = (int)g.M;
   p.N = (int)g.N;
   p.K = (int)g.K;
@@ -820,49 +858,62 @@ TileShape choose_tile(int64_t M, int64_t N, int sms) {
   return best;
 }
 
-template <bool PROMOTE, bool OUT_BF16, bool B_TILE>
+template <bool PROMOTE, int OUT, bool B_TILE>
 cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
+  // E4M3 output needs each promotion thread to own one whole 1x128 group:
+  // 128 x 256 tiles (two 128-column halves per row)
+  if constexpr (OUT == kOutE4m3) {
+    return launch_variant<256, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
+  } else {
   int shape = g.tile;
   if (shape < 0) shape = choose_tile(g.M, g.N, num_sms_current_device());
   switch (shape) {
     case kTile128x192x2W12:
-      return launch_variant<192, 2, false, 12, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<192, 2, false, 12, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile256x192PairW12:
-      return launch_variant<192, 2, true, 12, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<192, 2, true, 12, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile256x128Pair:
-      return launch_variant<128, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<128, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile256x160Pair:
-      return launch_variant<160, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<160, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile256x256Pair:
-      return launch_variant<256, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<256, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile256x224Pair:
-      return launch_variant<224, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<224, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile256x192Pair:
-      return launch_variant<192, 2, true, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<192, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile128x256x2:
-      return launch_variant<256, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<256, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile128x224x2:
-      return launch_variant<224, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<224, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile128x192x2:
-      return launch_variant<192, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<192, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile128x160x2:
-      return launch_variant<160, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<160, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
     case kTile128x128x2:
-      return launch_variant<128, 2, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
+      return launch_variant<128, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
     default:
-      return launch_variant<128, 1, false, 8, PROMOTE, OUT_BF16, B_TILE>(g, stream);
-  }
+      return launch_variant<128, 1, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
+  }  }
 }
 
-template <bool PROMOTE, bool OUT_BF16>
+template <bool PROMOTE, int OUT>
 cudaError_t launch_bt(const GemmArgs& g, cudaStream_t stream) {
-  return g.b_tile ? launch_shape<PROMOTE, OUT_BF16, true>(g, stream)
-                  : launch_shape<PROMOTE, OUT_BF16, false>(g, stream);
+  return g.b_tile ? launch_shape<PROMOTE, OUT, true>(g, stream)
+                  : launch_shape<PROMOTE, OUT, false>(g, stream);
 }
 
 template <bool PROMOTE>
 cudaError_t launch_out(const GemmArgs& g, cudaStream_t stream) {
-  return g.out_bf16 ? launch_bt<PROMOTE, true>(g, stream) : launch_bt<PROMOTE, false>(g, stream);
+  switch (g.out) {
+    case kOutBf16:
+      return launch_bt<PROMOTE, kOutBf16>(g, stream);
+    case kOutE4m3:
+      if constexpr (PROMOTE) return launch_bt<PROMOTE, kOutE4m3>(g, stream);
+      return cudaErrorInvalidValue;
+    default:
+      return launch_bt<PROMOTE, kOutF32>(g, stream);
+  }
 }
 
 }  // namespace

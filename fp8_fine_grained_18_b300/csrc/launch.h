@@ -18,8 +18,14 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, uint8_t*
                                    cudaStream_t stream);
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t* qT, float* sT,
                                    cudaStream_t stream);
+cudaError_t launch_quant_act_dual(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
+                                  uint8_t* qT, float* sT, cudaStream_t stream);
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
                                         uint8_t* qT, float* sT, cudaStream_t stream);
+// Per-tensor scale of n bf16 values (n % 8 == 0): q codes, *scale, and
+// n_bcast copies of the scale in bcast (nullable when n_bcast == 0).
+cudaError_t launch_quant_per_tensor(const void* x, int64_t n, uint8_t* q, float* scale,
+                                    float* bcast, int64_t n_bcast, cudaStream_t stream);
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                           uint8_t* qT, float* sT, cudaStream_t stream);
 
@@ -31,7 +37,8 @@ struct GemmArgs {
   bool b_tile;  // B scales per 1x128 tile (else per 128x128 block)
   int64_t M, N, K;
   void* c;
-  bool out_bf16;
+  float* c_scales;  // E4M3 output only: [N/128][M]
+  int out;          // 0 FP32, 1 BF16, 2 E4M3 codes + 1x128 scales
   bool promote;
   int skip_iter;  // test hook: producer skips this pipeline iteration (-1: never)
   int tile;       // fp8bs_tile_shape value; -1 chooses per problem shape

@@ -60,29 +60,6 @@ __device__ __forceinline__ bool pair_has_nan(uint32_t m) {
   return (m & 0xFFFFu) > kBf16Inf || (m >> 16) > kBf16Inf;
 }
 
-// Max of |x| that propagates NaN (a NaN in the group shows up as NaN).
-__device__ __forceinline__ float fmax_abs_nan(float acc, float x) {
-  float r;
-  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(acc), "f"(fabsf(x)));
-  return r;
-}
-
-struct GroupScale {
-  float s, nr;  // scale, and -fl32(1 / s) on the fast path
-  bool fast;
-};
-
-// Scale of a group from its amax given as a bit pattern (bf16 when bf16 is
-// true, else FP32); special = the group holds Inf or NaN.
-__device__ __forceinline__ GroupScale make_scale(uint32_t mag_no_nan_bits, bool special,
-                                                 bool bf16) {
-  GroupScale g;
-  g.s = group_scale(__uint_as_float(bf16 ? mag_no_nan_bits << 16 : mag_no_nan_bits));
-  g.fast = !special && g.s >= kFastScaleMin;
-  g.nr = g.fast ? -__frcp_rn(g.s) : 0.0f;
-  return g;
-}
-
 // Four bf16 (two words, element 0 in the low half of wa) -> four codes,
 // element 0 in byte 0.  The fast path converts the negated quotients and
 // flips the four sign bits at once.
@@ -101,18 +78,6 @@ __device__ __forceinline__ uint32_t codes_bf16x4(uint32_t wa, uint32_t wb, const
 // Eight bf16 (one 16-byte vector) -> eight codes in two words.
 __device__ __forceinline__ uint2 codes_bf16x8(uint4 v, const GroupScale& g) {
   return make_uint2(codes_bf16x4(v.x, v.y, g), codes_bf16x4(v.z, v.w, g));
-}
-
-// Four FP32 values (full 24-bit significands) -> four codes.
-__device__ __forceinline__ uint32_t codes_f32x4(float a, float b, float c, float d,
-                                                const GroupScale& g) {
-  if (g.fast) {
-    const float2 q0 = neg_quotient_2step_x2(make_float2(a, b), g.s, g.nr);
-    const float2 q1 = neg_quotient_2step_x2(make_float2(c, d), g.s, g.nr);
-    return (e4m3x2(q0.x, q0.y) | (e4m3x2(q1.x, q1.y) << 16)) ^ 0x80808080u;
-  }
-  return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s)) |
-         (e4m3x2_nan(quotient_general(c, g.s), quotient_general(d, g.s)) << 16);
 }
 
 __device__ __forceinline__ GroupScale shfl_scale(const GroupScale& g, int src) {
@@ -464,12 +429,102 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// Per-tensor baseline: one scale for the whole tensor, from its max-abs
+// mapped to the FP8 maximum (the standard practice that the fine-grained
+// tiles replace, kept to measure what they gain).  Three stream-ordered
+// launches with no scratch memory: pass 1 folds the NaN-free bf16 magnitudes
+// into the caller's scale word with one atomicMax per CTA (the FP32 bits of
+// non-negative values order like unsigned integers, and a bf16 magnitude
+// shifted left by 16 is its FP32 bit pattern); pass 2 quantizes with
+// s = fl32(amax / 448) and writes the optional broadcast copy of s; pass 3,
+// one thread, replaces the amax in the scale word by s.
+// ---------------------------------------------------------------------------
+constexpr int kPtThreads = 512;
+constexpr int kPtCtasPerSm = 4;  // 2048 threads per SM
+
+// The two bf16 magnitudes of a word, NaN lanes set to zero.
+__device__ __forceinline__ uint32_t mag_no_nan2(uint32_t w) {
+  const uint32_t mag = w & 0x7FFF7FFFu;
+  return mag & ~__vcmpgtu2(mag, 0x7F807F80u);
+}
+
+__device__ __forceinline__ uint32_t mag_max8(const uint4& v) {
+  return __vmaxu2(__vmaxu2(mag_no_nan2(v.x), mag_no_nan2(v.y)),
+                  __vmaxu2(mag_no_nan2(v.z), mag_no_nan2(v.w)));
+}
+
+__device__ __forceinline__ bool has_nan8(const uint4& v) {
+  const uint32_t inf2 = 0x7F807F80u;
+  return (__vcmpgtu2(v.x & 0x7FFF7FFFu, inf2) | __vcmpgtu2(v.y & 0x7FFF7FFFu, inf2) |
+          __vcmpgtu2(v.z & 0x7FFF7FFFu, inf2) | __vcmpgtu2(v.w & 0x7FFF7FFFu, inf2)) != 0;
+}
+
+__global__ void __launch_bounds__(kPtThreads) tensor_amax_kernel(const uint4* __restrict__ x,
+                                                                 int64_t nvec,
+                                                                 unsigned int* amax_bits) {
+  uint32_t m2 = 0;
+  const int64_t stride = (int64_t)gridDim.x * kPtThreads;
+  int64_t i = (int64_t)blockIdx.x * kPtThreads + threadIdx.x;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {  // four 16-byte loads in flight
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = ld_stream_v4(x + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m2 = __vmaxu2(m2, mag_max8(v[u]));
+  }
+  for (; i < nvec; i += stride) m2 = __vmaxu2(m2, mag_max8(ld_stream_v4(x + i)));
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  m = __reduce_max_sync(kFull, m);
+  __shared__ uint32_t red[kPtThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t r = lane < kPtThreads / 32 ? red[lane] : 0u;
+    r = __reduce_max_sync(kFull, r);
+    if (lane == 0 && r != 0u) atomicMax(amax_bits, r << 16);
+  }
+}
+
+__global__ void __launch_bounds__(kPtThreads) tensor_quant_kernel(const uint4* __restrict__ x,
+                                                                  int64_t nvec,
+                                                                  uint2* __restrict__ q,
+                                                                  const float* amax_word,
+                                                                  float* __restrict__ bcast,
+                                                                  int64_t n_bcast) {
+  const uint32_t abits = __float_as_uint(*amax_word);
+  const GroupScale g = make_scale(abits, abits >= 0x7F800000u, false);
+  GroupScale g_slow = g;
+  g_slow.fast = false;
+  const int64_t stride = (int64_t)gridDim.x * kPtThreads;
+  const int64_t t0 = (int64_t)blockIdx.x * kPtThreads + threadIdx.x;
+  int64_t i = t0;
+  for (; i + stride < nvec; i += 2 * stride) {
+    const uint4 v0 = ld_stream_v4(x + i), v1 = ld_stream_v4(x + i + stride);
+    q[i] = codes_bf16x8(v0, has_nan8(v0) ? g_slow : g);
+    q[i + stride] = codes_bf16x8(v1, has_nan8(v1) ? g_slow : g);
+  }
+  for (; i < nvec; i += stride) {
+    const uint4 v = ld_stream_v4(x + i);
+    q[i] = codes_bf16x8(v, has_nan8(v) ? g_slow : g);
+  }
+  for (int64_t j = t0; j < n_bcast; j += stride) bcast[j] = g.s;
+}
+
+__global__ void tensor_scale_finalize_kernel(float* scale_word) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) *scale_word = group_scale(*scale_word);
+}
+
 // Q1T: 128x1 tiles (128 consecutive rows of one column), output transposed.
 // Thread (cp, part): column pair cp (0..63), rows 32 part .. 32 part + 31.
-// grid = (K/128, M/128).
+// With DUAL the same shared-memory tile also yields the 1x128 tiles of its
+// rows (q, s, as Q1 writes them): grad_out quantized both ways from one
+// read.  grid = (K/128, M/128).
+template <bool DUAL>
 __global__ void __launch_bounds__(256) quant_act_128x1_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t K, uint8_t* __restrict__ qT,
-    float* __restrict__ sT) {
+    float* __restrict__ sT, uint8_t* __restrict__ q, float* __restrict__ s) {
   __shared__ uint4 tile[128 * 16];  // row r, 16-byte segment g at [r * 16 + g]
   __shared__ uint32_t red[4][64];
   const int t = threadIdx.x;
@@ -482,6 +537,52 @@ __global__ void __launch_bounds__(256) quant_act_128x1_kernel(
     tile[idx] = ld_stream_v4(x + (m0 + (idx >> 4)) * K + k0 + (idx & 15) * 8);
   }
   __syncthreads();
+  if constexpr (DUAL) {
+    // 1x128 tiles: half-warp h owns rows h, h + 16, ..., h + 112; lane l of
+    // it holds 8 consecutive elements of each, and lanes 0..7 compute the
+    // eight rows' scales.
+    const int hw = t >> 4, l16 = t & 15;
+    uint4 v[8];
+    uint32_t mrow[8], prow[8];
+    bool nan_seen = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[i] = tile[(hw + 16 * i) * 16 + l16];
+      uint32_t mm = halves_max(mag_pair_max(
+          mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y), v[i].z), v[i].w));
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
+      prow[i] = mrow[i] = mm;
+      nan_seen |= mm > kBf16Inf;
+    }
+    if (__any_sync(kFull, nan_seen)) {  // rare: recount without NaN
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t mm = halves_max(mag_pair_max_no_nan(
+            mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
+                                v[i].z),
+            v[i].w));
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
+        mrow[i] = mm;
+      }
+    }
+    uint32_t mj = 0, pj = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((l16 & 7) == i) {
+        mj = mrow[i];
+        pj = prow[i];
+      }
+    const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const GroupScale g = shfl_scale(mine, (t & 16) + i);
+      const int64_t r = m0 + hw + 16 * i;
+      *reinterpret_cast<uint2*>(q + r * K + k0 + l16 * 8) = codes_bf16x8(v[i], g);
+      if (l16 == i) s[(k0 / kGroup) * M + r] = mine.s;
+    }
+  }
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
   const int cp = t & 63, part = t >> 6;
   uint32_t m = 0;
@@ -645,7 +746,16 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, uint8_t*
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t* qT, float* sT,
                                    cudaStream_t stream) {
   dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
-  quant_act_128x1_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K, qT, sT);
+  quant_act_128x1_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
+                                                           qT, sT, nullptr, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_dual(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
+                                  uint8_t* qT, float* sT, cudaStream_t stream) {
+  dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
+  quant_act_128x1_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
+                                                          qT, sT, q, s);
   return cudaGetLastError();
 }
 
@@ -670,6 +780,25 @@ cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int6
                                           uint8_t* qT, float* sT, cudaStream_t stream) {
   dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
   requant_1x128_to_128x1_kernel<<<grid, 256, 0, stream>>>(q, s, M, K, qT, sT);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_per_tensor(const void* x, int64_t n, uint8_t* q, float* scale,
+                                    float* bcast, int64_t n_bcast, cudaStream_t stream) {
+  const int64_t nvec = n / 8;
+  cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int64_t max_grid = (int64_t)num_sms_current_device() * kPtCtasPerSm;
+  int64_t g1 = (nvec + kPtThreads - 1) / kPtThreads;
+  g1 = g1 < 1 ? 1 : (g1 > max_grid ? max_grid : g1);
+  const auto* xv = static_cast<const uint4*>(x);
+  tensor_amax_kernel<<<(unsigned)g1, kPtThreads, 0, stream>>>(
+      xv, nvec, reinterpret_cast<unsigned int*>(scale));
+  int64_t g2 = ((nvec > n_bcast ? nvec : n_bcast) + kPtThreads - 1) / kPtThreads;
+  g2 = g2 < 1 ? 1 : (g2 > max_grid ? max_grid : g2);
+  tensor_quant_kernel<<<(unsigned)g2, kPtThreads, 0, stream>>>(
+      xv, nvec, reinterpret_cast<uint2*>(q), scale, bcast, n_bcast);
+  tensor_scale_finalize_kernel<<<1, 32, 0, stream>>>(scale);
   return cudaGetLastError();
 }
 

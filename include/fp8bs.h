@@ -63,7 +63,12 @@ typedef enum {
   FP8BS_ERR_TIMEOUT = 6            /* a bounded device wait gave up */
 } fp8bs_status;
 
-typedef enum { FP8BS_OUT_BF16 = 0, FP8BS_OUT_F32 = 1 } fp8bs_out_dtype;
+/* E4M3_1x128 is only for fp8bs_gemm_quant_out (it needs a scale array). */
+typedef enum {
+  FP8BS_OUT_BF16 = 0,
+  FP8BS_OUT_F32 = 1,
+  FP8BS_OUT_E4M3_1x128 = 2
+} fp8bs_out_dtype;
 
 typedef enum {
   /* B scales per 128x128 block: sb[N/128][K/128] (forward, input-grad) */
@@ -89,6 +94,21 @@ typedef enum {
 fp8bs_status fp8bs_quant_act_1x128(const void *x_bf16, int64_t M, int64_t K,
                                    int transpose_out, uint8_t *q,
                                    float *scales, fp8bs_stream_t stream);
+
+/*
+ * Both activation tilings of one tensor from a single read [P1¶3]: the
+ * 1x128 tiles of fp8bs_quant_act_1x128(transpose_out = 0) and the 128x1
+ * tiles of fp8bs_quant_act_1x128(transpose_out = 1), bit-identical to those
+ * two calls.  Meant for grad_out, which feeds the input-gradient GEMM as
+ * 1x128 tiles and the weight-gradient GEMM as 128x1 tiles; it reads the bf16
+ * input from HBM once instead of twice.
+ *   x: bf16 [M][K] -> q: E4M3 [M][K], scales: f32 [K/128][M]
+ *                  -> qT: E4M3 [K][M], scalesT: f32 [M/128][K].
+ *   Requires M % 128 == 0 and K % 128 == 0.
+ */
+fp8bs_status fp8bs_quant_act_dual(const void *x_bf16, int64_t M, int64_t K,
+                                  uint8_t *q, float *scales, uint8_t *qT,
+                                  float *scalesT, fp8bs_stream_t stream);
 
 /*
  * Weight quantizer [P1¶3]: one scale per 128x128 block of W.
@@ -195,6 +215,46 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *a, const float *sa,
                               int64_t K, void *c, fp8bs_out_dtype out,
                               int promote, fp8bs_tile_shape tile,
                               fp8bs_stream_t stream);
+
+/*
+ * Per-tensor FP8 quantization: the standard practice that the fine-grained
+ * tiles replace [P1¶4][P3¶4] (one scale for the whole tensor, its max-abs
+ * mapped to the FP8 maximum; sensitive to outliers).  Kept as the accuracy
+ * baseline; the rule per element is that of fp8bs_quant_act_1x128 with a
+ * single group: s = fl32(amax / 448), code = E4M3_RNE_satfinite(fl32(x / s)),
+ * amax ignoring NaN.
+ *   x: bf16 [rows][cols] -> q: E4M3 [rows][cols];
+ *   scale: one float (device), written with s (it holds the running max
+ *     while the call is in flight);
+ *   scales_bcast (nullable when n_bcast == 0): n_bcast floats, each set to
+ *     s, so q can go to fp8bs_gemm with any of its scale layouts (as A:
+ *     [cols/128][rows]; as B with BLOCK scales: [rows/128][cols/128]).
+ *   Requires cols % 16 == 0; x and q 16-byte aligned, scale and
+ *   scales_bcast 4-byte aligned.  rows == 0 or cols == 0 is a no-op.
+ *   Three launches and one 4-byte memset on `stream`; no scratch memory.
+ */
+fp8bs_status fp8bs_quant_per_tensor(const void *x_bf16, int64_t rows,
+                                    int64_t cols, uint8_t *q, float *scale,
+                                    float *scales_bcast, int64_t n_bcast,
+                                    fp8bs_stream_t stream);
+
+/*
+ * The block-scaled GEMM with its output quantized in the epilogue, for the
+ * next layer [P2¶1: the BF16 result otherwise makes a round trip through HBM
+ * before it is quantized].  Computes the FP32 C of fp8bs_gemm (promoted),
+ * then quantizes each 1x128 tile of each C row by the rule of
+ * fp8bs_quant_act_1x128 applied to the FP32 values: s = fl32(amax / 448),
+ * code = E4M3_RNE_satfinite(fl32(C / s)).
+ *   c: E4M3 [M][N], c_scales: f32 [N/128][M] (the layout of
+ *   fp8bs_quant_act_1x128's output, so c can feed the next GEMM as its A).
+ *   Requires N % 128 == 0 (and the fp8bs_gemm requirements); always uses
+ *   128 x 256 output tiles.
+ */
+fp8bs_status fp8bs_gemm_quant_out(const uint8_t *a, const float *sa,
+                                  const uint8_t *b, const float *sb,
+                                  fp8bs_bscale_kind bkind, int64_t M,
+                                  int64_t N, int64_t K, uint8_t *c,
+                                  float *c_scales, fp8bs_stream_t stream);
 
 /* Static English name of a status code. */
 const char *fp8bs_status_string(fp8bs_status status);

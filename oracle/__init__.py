@@ -37,6 +37,8 @@ def lib():
         L.fp8bs_oracle_double_to_bf16.argtypes = [ctypes.c_double]
         L.fp8bs_oracle_quant_act_1x128.argtypes = [P, I, I, P, P]
         L.fp8bs_oracle_quant_act_128x1.argtypes = [P, I, I, P, P]
+        L.fp8bs_oracle_quant_f32_1x128.argtypes = [P, I, I, P, P]
+        L.fp8bs_oracle_quant_per_tensor.argtypes = [P, I, I, P, P]
         L.fp8bs_oracle_quant_weight_128x128.argtypes = [P, I, I, P, P, P, P]
         L.fp8bs_oracle_requant_1x128_to_128x1.argtypes = [P, P, I, I, P, P]
         L.fp8bs_oracle_quant_rowwise.argtypes = [P, I, I, P, P]
@@ -46,8 +48,8 @@ def lib():
             P, P, P, P, ctypes.c_int, I, I, I, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, P, P, I, P]
         L.fp8bs_oracle_num_threads.restype = ctypes.c_int
-        for f in ("quant_act_1x128", "quant_act_128x1", "quant_weight_128x128",
-                  "requant_1x128_to_128x1", "quant_rowwise", "gemm",
+        for f in ("quant_act_1x128", "quant_act_128x1", "quant_f32_1x128", "quant_weight_128x128",
+                  "requant_1x128_to_128x1", "quant_rowwise", "quant_per_tensor", "gemm",
                   "gemm_sampled", "gemm_limited_acc"):
             getattr(L, "fp8bs_oracle_" + f).restype = None
         _lib = L
@@ -105,6 +107,26 @@ def quant_act_1x128(x_bf16: np.ndarray):
     q = np.empty((M, K), np.uint8)
     s = np.empty((K // GROUP, M), np.float32)
     lib().fp8bs_oracle_quant_act_1x128(_p(x), M, K, _p(q), _p(s))
+    return q, s
+
+
+def quant_per_tensor(x_bf16: np.ndarray):
+    """bf16 bits [rows, cols] -> (q uint8 [rows, cols], s float32 scalar)."""
+    x = _c(x_bf16, np.uint16)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), np.uint8)
+    s = np.empty(1, np.float32)
+    lib().fp8bs_oracle_quant_per_tensor(_p(x), rows, cols, _p(q), _p(s))
+    return q, s[0]
+
+
+def quant_f32_1x128(x: np.ndarray):
+    """x: float32 [M, K] -> (q uint8 [M, K], s float32 [K/128, M])."""
+    x = _c(x, np.float32)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // GROUP, M), np.float32)
+    lib().fp8bs_oracle_quant_f32_1x128(_p(x), M, K, _p(q), _p(s))
     return q, s
 
 

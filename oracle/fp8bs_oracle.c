@@ -142,6 +142,35 @@ void fp8bs_oracle_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K,
   }
 }
 
+void fp8bs_oracle_quant_f32_1x128(const float *x, int64_t M, int64_t K,
+                                  uint8_t *q, float *s) {
+  int64_t KB = K / GROUP;
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t kb = 0; kb < KB; ++kb) {
+      const float *row = x + m * K + kb * GROUP;
+      float amax = 0.0f;
+      for (int j = 0; j < GROUP; ++j) amax = amax_update(amax, row[j]);
+      float sc = scale_of(amax);
+      s[kb * M + m] = sc;
+      for (int j = 0; j < GROUP; ++j) q[m * K + kb * GROUP + j] = code_of(row[j], sc);
+    }
+  }
+}
+
+void fp8bs_oracle_quant_per_tensor(const uint16_t *x, int64_t rows,
+                                   int64_t cols, uint8_t *q, float *s) {
+  int64_t n = rows * cols;
+  float amax = 0.0f;
+  for (int64_t i = 0; i < n; ++i)
+    amax = amax_update(amax, fp8bs_oracle_bf16_to_float(x[i]));
+  float sc = scale_of(amax);
+  *s = sc;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i)
+    q[i] = code_of(fp8bs_oracle_bf16_to_float(x[i]), sc);
+}
+
 void fp8bs_oracle_quant_act_128x1(const uint16_t *x, int64_t M, int64_t N,
                                   uint8_t *qT, float *sT) {
   /* Literally: transpose, then 1x128 tiles along the new rows. */

@@ -72,6 +72,19 @@ uint16_t fp8bs_oracle_double_to_bf16(double v);
 void fp8bs_oracle_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K,
                                   uint8_t *q, float *s);
 
+/* [P1¶3] the 1x128 rule applied to FP32 values (the output of a GEMM that is
+ * quantized for the next layer): x: float [M][K], K % 128 == 0.
+ * q: [M][K].  s: [K/128][M]. */
+void fp8bs_oracle_quant_f32_1x128(const float *x, int64_t M, int64_t K,
+                                  uint8_t *q, float *s);
+
+/* [P1¶4][P3¶4] the standard practice the fine-grained tiles replace: one
+ * scale for the whole tensor, its max-abs mapped to the FP8 maximum (the
+ * accuracy baseline).  x: bf16 bits [rows][cols]; q: [rows][cols];
+ * *s: the one scale (readings R2-R5 with a single group). */
+void fp8bs_oracle_quant_per_tensor(const uint16_t *x, int64_t rows,
+                                   int64_t cols, uint8_t *q, float *s);
+
 /* [P1¶3] the same tiles laid along the other axis (128x1): groups are 128
  * consecutive rows of one column.  Equals quant_act_1x128 applied to the
  * transpose of x.  x: bf16 bits [M][N], M % 128 == 0.

@@ -28,7 +28,8 @@ def _declared_functions():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("fp8bs_quant_act_1x128", "fp8bs_quant_weight_128x128",
-                     "fp8bs_requant_1x128_to_128x1", "fp8bs_gemm", "fp8bs_gemm_ex",
+                     "fp8bs_requant_1x128_to_128x1", "fp8bs_quant_act_dual", "fp8bs_gemm",
+                     "fp8bs_gemm_ex", "fp8bs_gemm_quant_out", "fp8bs_quant_per_tensor",
                      "fp8bs_status_string", "fp8bs_get_device_error"):
         assert required in names
 
@@ -66,7 +67,20 @@ def test_quant_argument_errors(libfp8bs):
     assert L.fp8bs_quant_weight_128x128(FAKE, 100, 128, FAKE, FAKE, None, None, None) == m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_quant_weight_128x128(FAKE, 128, 128, FAKE, FAKE_ODD, None, None, None) == m.ERR_MISALIGNED
     assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 128, 128, FAKE, None, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_quant_act_dual(None, 0, 128, None, None, None, None, None) == m.OK
+    assert L.fp8bs_quant_act_dual(FAKE, 128, 128, FAKE, FAKE, FAKE, None, None) == m.ERR_INVALID_ARG
+    assert L.fp8bs_quant_act_dual(FAKE, 100, 128, FAKE, FAKE, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_dual(FAKE, 128, 128, FAKE_ODD, FAKE, FAKE, FAKE, None) == m.ERR_MISALIGNED
     assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 129, 128, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    pt = L.fp8bs_quant_per_tensor
+    assert pt(None, 0, 16, None, None, None, 0, None) == m.OK
+    assert pt(FAKE, -1, 16, FAKE, FAKE, None, 0, None) == m.ERR_INVALID_ARG
+    assert pt(FAKE, 4, 16, FAKE, FAKE, None, 5, None) == m.ERR_INVALID_ARG      # n_bcast without array
+    assert pt(FAKE, 4, 16, FAKE, FAKE, FAKE, -1, None) == m.ERR_INVALID_ARG
+    assert pt(FAKE, 4, 16, FAKE, None, None, 0, None) == m.ERR_INVALID_ARG
+    assert pt(FAKE, 4, 24, FAKE, FAKE, None, 0, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert pt(FAKE_ODD, 4, 16, FAKE, FAKE, None, 0, None) == m.ERR_MISALIGNED
+    assert pt(FAKE, 4, 16, FAKE, ctypes.c_void_p(0x10002), None, 0, None) == m.ERR_MISALIGNED
 
 
 def test_gemm_argument_errors(libfp8bs):
@@ -78,6 +92,14 @@ def test_gemm_argument_errors(libfp8bs):
     assert L.fp8bs_gemm_ex(*args(-1, 256, 128)) == m.ERR_INVALID_ARG
     assert L.fp8bs_gemm_ex(*args(8, 256, 128, bk=2)) == m.ERR_INVALID_ARG
     assert L.fp8bs_gemm_ex(*args(8, 256, 128, out=3)) == m.ERR_INVALID_ARG
+    # E4M3 output needs the scale array: only fp8bs_gemm_quant_out gives one
+    assert L.fp8bs_gemm_ex(*args(8, 256, 128, out=m.OUT_E4M3_1x128)) == m.ERR_INVALID_ARG
+    qargs = lambda M, N, K, cs=FAKE: (FAKE, FAKE, FAKE, FAKE, 0, M, N, K, FAKE, cs, None)  # noqa: E731
+    assert L.fp8bs_gemm_quant_out(*qargs(0, 256, 128)) == m.OK
+    assert L.fp8bs_gemm_quant_out(*qargs(8, 256, 128, cs=None)) == m.ERR_INVALID_ARG
+    assert L.fp8bs_gemm_quant_out(*qargs(8, 144, 128)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_quant_out(*qargs(8, 256, 100)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_quant_out(*qargs(8, 256, 128, cs=FAKE_ODD)) == m.ERR_MISALIGNED
     assert L.fp8bs_gemm_ex(*args(8, 256, 128, pr=2)) == m.ERR_INVALID_ARG
     assert L.fp8bs_gemm_ex(*args(8, 256, 128, a=None)) == m.ERR_INVALID_ARG
     assert L.fp8bs_gemm_ex(*args(8, 256, 100)) == m.ERR_UNSUPPORTED_SHAPE

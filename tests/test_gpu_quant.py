@@ -95,6 +95,35 @@ def test_act_128x1_special_values(fp8bs, oracle_mod):
     assert_scales_equal(sT, rs, "scales")
 
 
+@pytest.mark.parametrize("M,K,seed", [(128, 128, 0), (256, 384, 1), (512, 1024, 2), (384, 2048, 3)])
+def test_act_dual(fp8bs, oracle_mod, M, K, seed):
+    """One read, both tilings: bit-identical to the 1x128 and the 128x1 quantizer."""
+    rng = np.random.default_rng(40 + seed)
+    x, _ = synth.normal_with_outlier_columns(rng, (M, K), 3, 50.0)
+    q, s, qT, sT = fp8bs.quant_act_dual(dev_bf16(x))
+    rq, rs = oracle_mod.quant_act_1x128(x)
+    rqT, rsT = oracle_mod.quant_act_128x1(x)
+    assert_codes_equal(q, rq, "codes 1x128")
+    assert_scales_equal(s, rs, "scales 1x128")
+    assert_codes_equal(qT, rqT, "codes 128x1")
+    assert_scales_equal(sT, rsT, "scales 128x1")
+
+
+def test_act_dual_special_values(fp8bs, oracle_mod):
+    rows = _special_rows(256)  # 6 rows x 256
+    x = np.zeros((256, 256), np.uint16)
+    for i in range(256):
+        x[i] = rows[(i * 5) % 6]
+    x[:, 7] = rows[2][:256]  # a column with NaN/Inf
+    q, s, qT, sT = fp8bs.quant_act_dual(dev_bf16(x))
+    rq, rs = oracle_mod.quant_act_1x128(x)
+    rqT, rsT = oracle_mod.quant_act_128x1(x)
+    assert_codes_equal(q, rq, "codes 1x128")
+    assert_scales_equal(s, rs, "scales 1x128")
+    assert_codes_equal(qT, rqT, "codes 128x1")
+    assert_scales_equal(sT, rsT, "scales 128x1")
+
+
 @pytest.mark.parametrize("N,K,seed", [(128, 128, 0), (256, 640, 1), (1024, 384, 2)])
 def test_weight_128x128(fp8bs, oracle_mod, N, K, seed):
     rng = np.random.default_rng(seed)
@@ -174,6 +203,13 @@ def test_backward_quantizers_full(fp8bs, oracle_mod):
     rqT, rsT = oracle_mod.quant_act_128x1(inp["dY"])
     assert_codes_equal(qT, rqT, "dY^T codes")
     assert_scales_equal(sT, rsT, "dY^T scales")
+    # both tilings of grad_out from one read
+    q2, s2, qT2, sT2 = fp8bs.quant_act_dual(dev_bf16(inp["dY"]))
+    rq2, rs2 = oracle_mod.quant_act_1x128(inp["dY"])
+    assert_codes_equal(q2, rq2, "dY codes (dual)")
+    assert_scales_equal(s2, rs2, "dY scales (dual)")
+    assert_codes_equal(qT2, rqT, "dY^T codes (dual)")
+    assert_scales_equal(sT2, rsT, "dY^T scales (dual)")
     # cached activation X: 1x128 then re-tiled to 128x1
     qx, sx = fp8bs.quant_act_1x128(dev_bf16(inp["X"]))
     rqx, rsx = oracle_mod.quant_act_1x128(inp["X"])

@@ -9,6 +9,7 @@ import os
 import numpy as np
 import pytest
 
+import synth
 from synth import f32_to_bf16_bits, bf16_bits_to_f32, normal, normal_with_outlier_columns
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "e4m3_hand_tiles.txt")
@@ -206,3 +207,88 @@ def test_rowwise(oracle_mod):
     for kb in range(4):
         assert np.array_equal(s[kb], (amax / np.float32(448)).astype(np.float32))
     _check_invariants(oracle_mod, xf, q, np.repeat(s[:1].T, 512, axis=1))
+
+
+def test_f32_1x128_equals_bf16_rule_on_bf16_values(oracle_mod):
+    """On values that are exactly bf16 the FP32-input quantizer is the bf16
+    one (same rule, same arithmetic)."""
+    rng = np.random.default_rng(31)
+    bits, _ = synth.normal_with_outlier_columns(rng, (64, 512), 3, 100.0)
+    q16, s16 = oracle_mod.quant_act_1x128(bits)
+    q32, s32 = oracle_mod.quant_f32_1x128(synth.bf16_bits_to_f32(bits))
+    assert np.array_equal(q16, q32) and np.array_equal(s16.view(np.uint32), s32.view(np.uint32))
+
+
+def test_f32_1x128_invariants(oracle_mod):
+    """Full-precision FP32 inputs: every element within half an E4M3 step
+    (plus the FP32 quotient's rounding) of its dequantized code, and the
+    tile maximum maps to 448."""
+    rng = np.random.default_rng(32)
+    x = (rng.standard_normal((32, 256)) * 10.0 ** rng.uniform(-3, 3, (32, 1))).astype(np.float32)
+    x[3, :128] = 0.0
+    q, s = oracle_mod.quant_f32_1x128(x)
+    dec = oracle_mod.e4m3_decode_array(q)
+    for m in range(32):
+        for kb in range(2):
+            sc = float(s[kb, m])
+            xs = x[m, kb * 128:(kb + 1) * 128].astype(np.float64)
+            d = dec[m, kb * 128:(kb + 1) * 128]
+            if sc == 0.0:
+                assert np.all(d == 0.0)
+                continue
+            y = np.abs(xs / sc)
+            e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+            half_ulp = 0.5 * np.where(y < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+            assert np.all(np.abs(xs - d * sc) <= (half_ulp + 2.0 ** -24 * y) * sc + 1e-300)
+            assert np.max(np.abs(d)) == 448.0
+
+
+def _tiles_with_common_max(rng, rows, cols, peak):
+    """bf16 bits whose every 1x128 tile holds +-peak exactly once, the rest
+    N(0, 1) below it in magnitude."""
+    x = np.clip(rng.standard_normal((rows, cols)), -0.9 * peak, 0.9 * peak).astype(np.float32)
+    for kb in range(cols // 128):
+        j = rng.integers(0, 128, rows)
+        x[np.arange(rows), kb * 128 + j] = np.where(rng.random(rows) < 0.5, -peak, peak)
+    return f32_to_bf16_bits(x)
+
+
+def test_per_tensor_equals_1x128_when_every_tile_holds_the_max(oracle_mod):
+    """One scale for the tensor is the 1x128 scale of every tile when every
+    tile has the tensor's max-abs, so the codes must agree."""
+    rng = np.random.default_rng(41)
+    bits = _tiles_with_common_max(rng, 48, 384, 3.0)
+    q_t, s_t = oracle_mod.quant_per_tensor(bits)
+    q_g, s_g = oracle_mod.quant_act_1x128(bits)
+    assert np.all(s_g == s_t) and np.array_equal(q_t, q_g)
+    assert s_t == np.float32(3.0) / np.float32(448.0)
+
+
+def test_per_tensor_unit_scale_is_plain_encoding(oracle_mod):
+    """A tensor whose max-abs is 448 has scale 1, so each code is the plain
+    E4M3 rounding of the value (x / 1 = x)."""
+    rng = np.random.default_rng(42)
+    x = (rng.standard_normal((16, 64)) * 40.0).astype(np.float32)
+    x[3, 7] = -448.0
+    bits = f32_to_bf16_bits(np.clip(x, -448.0, 448.0))
+    q, s = oracle_mod.quant_per_tensor(bits)
+    assert s == np.float32(1.0)
+    vals = bf16_bits_to_f32(bits)
+    assert all(q.flat[i] == oracle_mod.e4m3_encode(float(vals.flat[i])) for i in range(vals.size))
+
+
+def test_per_tensor_specials_and_outlier(oracle_mod):
+    """NaN is ignored by the max and encodes as 0x7F; an all-zero tensor has
+    scale 0 and signed-zero codes; one outlier sets the scale of everything
+    (the outlier sensitivity that motivates the 1x128 tiles)."""
+    z = f32_to_bf16_bits(np.array([[0.0, -0.0] * 8], np.float32))
+    q, s = oracle_mod.quant_per_tensor(z)
+    assert s == 0.0 and np.array_equal(q[0], np.array([0x00, 0x80] * 8, np.uint8))
+    x = np.full((2, 16), 1.0, np.float32)
+    x[0, 0] = np.nan
+    x[1, 5] = 2.0 ** 20
+    q, s = oracle_mod.quant_per_tensor(f32_to_bf16_bits(x))
+    assert s == np.float32(2.0 ** 20) / np.float32(448.0)
+    assert q[0, 0] == 0x7F and q[1, 5] == 0x7E
+    # 1.0 / s = 448 * 2^-20 < 2^-9 / 2 (half the smallest subnormal): code 0
+    assert np.all(np.delete(q.ravel(), [0, 21]) == 0x00)
