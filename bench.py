@@ -463,6 +463,11 @@ def measure_rows(fp8bs, torch, dev, peaks):
     quant_row("Q1 moe A 8192x7168", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
               algorithmic_bytes_q1(8192, 7168))
     gemm_row("G1 moe 8192x4096x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
+    # per-tensor baseline quantizer: a max-abs pass and a quantize pass
+    qpt, spt, _ = fp8bs.quant_per_tensor(a)
+    quant_row("Q per-tensor moe A 8192x7168 (max-abs pass + quantize pass; 3 B/elt algorithmic)",
+              lambda: fp8bs.quant_per_tensor(a, q=qpt, scale=spt), 3 * 8192 * 7168 + 4)
+    del qpt, spt
     # the GEMM output quantized for the next layer: fused epilogue against
     # the BF16 output written to HBM and quantized by Q1 afterwards
     c8, cs8 = fp8bs.gemm_quant_out(qa, sa, qb, sb, 0)
