@@ -31,6 +31,14 @@ def lib():
         L.fp8bs_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         L.fp8bs_oracle_e4m3_encode.restype = ctypes.c_uint8
         L.fp8bs_oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.fp8bs_oracle_e5m6_decode.restype = ctypes.c_double
+        L.fp8bs_oracle_e5m6_decode.argtypes = [ctypes.c_uint16]
+        L.fp8bs_oracle_e5m6_encode.restype = ctypes.c_uint16
+        L.fp8bs_oracle_e5m6_encode.argtypes = [ctypes.c_float]
+        L.fp8bs_oracle_e5m6_pack.argtypes = [P, I, P]
+        L.fp8bs_oracle_e5m6_unpack.argtypes = [P, I, P]
+        L.fp8bs_oracle_quant_act_e5m6_1x128.argtypes = [P, I, I, P, P]
+        L.fp8bs_oracle_requant_e5m6_to_128x1.argtypes = [P, P, I, I, P, P]
         L.fp8bs_oracle_bf16_to_float.restype = ctypes.c_float
         L.fp8bs_oracle_bf16_to_float.argtypes = [ctypes.c_uint16]
         L.fp8bs_oracle_double_to_bf16.restype = ctypes.c_uint16
@@ -49,7 +57,8 @@ def lib():
             ctypes.c_int, P, P, I, P]
         L.fp8bs_oracle_num_threads.restype = ctypes.c_int
         for f in ("quant_act_1x128", "quant_act_128x1", "quant_f32_1x128", "quant_weight_128x128",
-                  "requant_1x128_to_128x1", "quant_rowwise", "quant_per_tensor", "gemm",
+                  "requant_1x128_to_128x1", "quant_rowwise", "quant_per_tensor", "gemm", "e5m6_pack", "e5m6_unpack",
+                  "quant_act_e5m6_1x128", "requant_e5m6_to_128x1",
                   "gemm_sampled", "gemm_limited_acc"):
             getattr(L, "fp8bs_oracle_" + f).restype = None
         _lib = L
@@ -78,6 +87,56 @@ def e4m3_decode(code: int) -> float:
 
 def e4m3_encode(y: float) -> int:
     return lib().fp8bs_oracle_e4m3_encode(float(np.float32(y)))
+
+
+def e5m6_decode(code: int) -> float:
+    return lib().fp8bs_oracle_e5m6_decode(int(code))
+
+
+def e5m6_encode(y: float) -> int:
+    return lib().fp8bs_oracle_e5m6_encode(float(np.float32(y)))
+
+
+def e5m6_decode_array(codes: np.ndarray) -> np.ndarray:
+    """Elementwise decode (float64) of 12-bit codes via the scalar definition."""
+    table = np.array([e5m6_decode(c) for c in range(4096)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint16) & 0xFFF]
+
+
+def e5m6_pack(codes: np.ndarray) -> np.ndarray:
+    """12-bit codes [..., n] (n even) -> bytes [..., 3n/2]."""
+    c = np.ascontiguousarray(codes, dtype=np.uint16)
+    out = np.empty(c.shape[:-1] + (c.shape[-1] // 2 * 3,), np.uint8)
+    lib().fp8bs_oracle_e5m6_pack(_p(c), c.size, _p(out))
+    return out
+
+
+def e5m6_unpack(packed: np.ndarray) -> np.ndarray:
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] // 3 * 2,), np.uint16)
+    lib().fp8bs_oracle_e5m6_unpack(_p(p), out.size, _p(out))
+    return out
+
+
+def quant_act_e5m6_1x128(x_bf16: np.ndarray):
+    """bf16 bits [M, K] -> (packed E5M6 uint8 [M, 3K/2], s float32 [K/128, M])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    packed = np.empty((M, K // 2 * 3), np.uint8)
+    s = np.empty((K // GROUP, M), np.float32)
+    lib().fp8bs_oracle_quant_act_e5m6_1x128(_p(x), M, K, _p(packed), _p(s))
+    return packed, s
+
+
+def requant_e5m6_to_128x1(packed: np.ndarray, s: np.ndarray):
+    """packed [M, 3K/2], s [K/128, M] -> (qT uint8 [K, M], sT float32 [M/128, K])."""
+    pk = _c(packed, np.uint8)
+    sc = _c(s, np.float32)
+    M, K = pk.shape[0], pk.shape[1] // 3 * 2
+    qT = np.empty((K, M), np.uint8)
+    sT = np.empty((M // GROUP, K), np.float32)
+    lib().fp8bs_oracle_requant_e5m6_to_128x1(_p(pk), _p(sc), M, K, _p(qT), _p(sT))
+    return qT, sT
 
 
 def bf16_to_float(bits: int) -> float:

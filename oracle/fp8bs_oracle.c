@@ -243,6 +243,134 @@ void fp8bs_oracle_requant_1x128_to_128x1(const uint8_t *q, const float *s,
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* E5M6 (readings R9-R12)                                                    */
+/* ------------------------------------------------------------------------ */
+
+#define E5M6_MAX 65024.0 /* (1 + 63/64) * 2^15, code 0x7BF */
+
+/* Layout S EEEEE MMMMMM, bias 15: (64 + m) * 2^(e-21) for e >= 1,
+ * m * 2^-20 for e == 0. */
+double fp8bs_oracle_e5m6_decode(uint16_t code) {
+  int sign = (code >> 11) & 1;
+  int e = (code >> 6) & 0x1F;
+  int m = code & 0x3F;
+  double v;
+  if (e == 31)
+    v = (m == 0) ? INFINITY : NAN;
+  else
+    v = (e == 0) ? ldexp((double)m, -20) : ldexp((double)(64 + m), e - 21);
+  return sign ? -v : v;
+}
+
+/* Codes 0x000..0x7BF are the non-negative finite values in increasing order:
+ * a binary search finds the neighbours of |y|, as for E4M3. */
+uint16_t fp8bs_oracle_e5m6_encode(float y) {
+  if (isnan(y)) return 0x7FF;
+  uint16_t sign = signbit(y) ? 0x800 : 0x000;
+  double a = fabs((double)y);
+  if (a >= E5M6_MAX) return (uint16_t)(sign | 0x7BF);
+  int lo = 0, hi = 0x7BF; /* decode(lo) <= a < decode(hi) */
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (fp8bs_oracle_e5m6_decode((uint16_t)mid) <= a)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  double below = a - fp8bs_oracle_e5m6_decode((uint16_t)lo);
+  double above = fp8bs_oracle_e5m6_decode((uint16_t)hi) - a;
+  int c;
+  if (below < above)
+    c = lo;
+  else if (above < below)
+    c = hi;
+  else
+    c = (lo & 1) ? hi : lo;
+  return (uint16_t)(sign | c);
+}
+
+void fp8bs_oracle_e5m6_pack(const uint16_t *codes, int64_t n, uint8_t *packed) {
+  for (int64_t i = 0; i < n; i += 2) {
+    uint32_t c0 = codes[i] & 0xFFF, c1 = codes[i + 1] & 0xFFF;
+    uint32_t bitsv = c0 | (c1 << 12); /* bits 12i .. 12i+23 of the stream */
+    packed[3 * (i / 2)] = (uint8_t)(bitsv & 0xFF);
+    packed[3 * (i / 2) + 1] = (uint8_t)((bitsv >> 8) & 0xFF);
+    packed[3 * (i / 2) + 2] = (uint8_t)((bitsv >> 16) & 0xFF);
+  }
+}
+
+void fp8bs_oracle_e5m6_unpack(const uint8_t *packed, int64_t n,
+                              uint16_t *codes) {
+  for (int64_t i = 0; i < n; i += 2) {
+    uint32_t bitsv = (uint32_t)packed[3 * (i / 2)] |
+                     ((uint32_t)packed[3 * (i / 2) + 1] << 8) |
+                     ((uint32_t)packed[3 * (i / 2) + 2] << 16);
+    codes[i] = (uint16_t)(bitsv & 0xFFF);
+    codes[i + 1] = (uint16_t)(bitsv >> 12);
+  }
+}
+
+/* R10: scale and code of one element under the E5M6 maximum. */
+static float scale_of_e5m6(float amax) { return amax / (float)E5M6_MAX; }
+
+static uint16_t code_of_e5m6(float x, float s) {
+  if (isnan(x)) return 0x7FF;
+  if (s == 0.0f) return signbit(x) ? 0x800 : 0x000;
+  return fp8bs_oracle_e5m6_encode(x / s);
+}
+
+void fp8bs_oracle_quant_act_e5m6_1x128(const uint16_t *x, int64_t M,
+                                       int64_t K, uint8_t *packed, float *s) {
+  int64_t KB = K / GROUP;
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    uint16_t codes[GROUP];
+    for (int64_t kb = 0; kb < KB; ++kb) {
+      const uint16_t *row = x + m * K + kb * GROUP;
+      float amax = 0.0f;
+      for (int j = 0; j < GROUP; ++j)
+        amax = amax_update(amax, fp8bs_oracle_bf16_to_float(row[j]));
+      float sc = scale_of_e5m6(amax);
+      s[kb * M + m] = sc;
+      for (int j = 0; j < GROUP; ++j)
+        codes[j] = code_of_e5m6(fp8bs_oracle_bf16_to_float(row[j]), sc);
+      /* a 128-element group starts on a whole byte: bit 12 * 128 * kb */
+      fp8bs_oracle_e5m6_pack(codes, GROUP,
+                             packed + m * (K / 2 * 3) + kb * (GROUP / 2 * 3));
+    }
+  }
+}
+
+void fp8bs_oracle_requant_e5m6_to_128x1(const uint8_t *packed, const float *s,
+                                        int64_t M, int64_t K, uint8_t *qT,
+                                        float *sT) {
+  int64_t MB = M / GROUP, KB = K / GROUP;
+#pragma omp parallel for schedule(static)
+  for (int64_t kb = 0; kb < KB; ++kb) {
+    float xh[GROUP][GROUP]; /* [row within the block][column] */
+    uint16_t codes[GROUP];
+    for (int64_t mb = 0; mb < MB; ++mb) {
+      for (int j = 0; j < GROUP; ++j) {
+        int64_t m = mb * GROUP + j;
+        fp8bs_oracle_e5m6_unpack(packed + m * (K / 2 * 3) + kb * (GROUP / 2 * 3),
+                                 GROUP, codes);
+        for (int c = 0; c < GROUP; ++c)
+          xh[j][c] = (float)fp8bs_oracle_e5m6_decode(codes[c]) * s[kb * M + m];
+      }
+      for (int c = 0; c < GROUP; ++c) {
+        int64_t k = kb * GROUP + c;
+        float amax = 0.0f;
+        for (int j = 0; j < GROUP; ++j) amax = amax_update(amax, xh[j][c]);
+        float sc = scale_of(amax);
+        sT[mb * K + k] = sc;
+        for (int j = 0; j < GROUP; ++j)
+          qT[k * M + mb * GROUP + j] = code_of(xh[j][c], sc);
+      }
+    }
+  }
+}
+
 void fp8bs_oracle_quant_rowwise(const uint16_t *x, int64_t M, int64_t K,
                                 uint8_t *q, float *s) {
   int64_t KB = K / GROUP;

@@ -106,6 +106,43 @@ void fp8bs_oracle_requant_1x128_to_128x1(const uint8_t *q, const float *s,
                                          int64_t M, int64_t K, uint8_t *qT,
                                          float *sT);
 
+/* --- E5M6 cache of the re-tiled activations ([P1¶3]: the activations that
+ * go from 1x128 to 128x1 tiles in the backward pass are kept in a custom
+ * E5M6 format).  Readings:
+ *   R9   E5M6 = sign, 5 exponent bits (bias 15), 6 mantissa bits.  Exponent
+ *        field 0 holds the subnormals m * 2^-20; field 31 is Inf (m == 0)
+ *        or NaN; the largest finite value is 1.984375 * 2^15 = 65024
+ *        (code 0x7BF).  Rounding is to nearest, ties to even, saturating
+ *        like R8; NaN encodes as 0x7FF.
+ *   R10  the cache keeps the 1x128 tiles: s = fl32(amax / 65024) and
+ *        code = E5M6(fl32(x / s)), R2-R6 with 65024 in place of 448.
+ *   R11  codes are stored as a little-endian 12-bit stream: element i of a
+ *        row occupies bits 12i .. 12i+11 of the row's 3K/2 bytes.
+ *   R12  the backward re-tiling decodes x^ = fl32(decode(code) * s) (one
+ *        rounding, as R7) and applies the 128x1 E4M3 rule to x^. */
+
+/* Value of a 12-bit E5M6 code, in double (exact); NaN codes give NaN. */
+double fp8bs_oracle_e5m6_decode(uint16_t code);
+
+/* Nearest E5M6 code to y (R9). */
+uint16_t fp8bs_oracle_e5m6_encode(float y);
+
+/* n codes (n even) <-> 3n/2 bytes (R11). */
+void fp8bs_oracle_e5m6_pack(const uint16_t *codes, int64_t n, uint8_t *packed);
+void fp8bs_oracle_e5m6_unpack(const uint8_t *packed, int64_t n,
+                              uint16_t *codes);
+
+/* [P1¶3] x: bf16 [M][K] (K % 128 == 0) -> packed E5M6 [M][3K/2] bytes and
+ * s: [K/128][M] (R10, R11). */
+void fp8bs_oracle_quant_act_e5m6_1x128(const uint16_t *x, int64_t M,
+                                       int64_t K, uint8_t *packed, float *s);
+
+/* [P1¶3] the E5M6 cache re-tiled for the weight gradient: packed [M][3K/2],
+ * s [K/128][M] -> qT: E4M3 [K][M], sT: [M/128][K] (R12); M % 128 == 0. */
+void fp8bs_oracle_requant_e5m6_to_128x1(const uint8_t *packed, const float *s,
+                                        int64_t M, int64_t K, uint8_t *qT,
+                                        float *sT);
+
 /* Test-only row-wise quantization (one group = a whole row of K); the
  * per-tensor/standard practice contrast of [P1¶4][P3¶4] applied per row.
  * Writes the row scale to every K-group slot: s: [K/128][M]. */
