@@ -494,6 +494,18 @@ def measure_rows(fp8bs, torch, dev, peaks):
     qxT, sxT = fp8bs.requant_1x128_to_128x1(qx, sx)
     quant_row("Q3 requant X 4096x2048", lambda: fp8bs.requant_1x128_to_128x1(qx, sx, qT=qxT, scalesT=sxT),
               algorithmic_bytes_q3(4096, 2048))
+    # E5M6 cache of X: with the forward E4M3 codes from the same read, and
+    # re-tiled into the Wgrad operand
+    e5 = fp8bs.quant_act_e5m6(x)
+    n_x = 4096 * 2048
+    quant_row("Q1+E5M6 X 4096x2048 (E4M3 codes and E5M6 cache, one read)",
+              lambda: fp8bs.quant_act_e5m6(x, packed=e5[0], scales=e5[1], q=e5[2], q_scales=e5[3]),
+              int(n_x * (2 + 1 + 1.5 + 8 / 128)))
+    q5T, s5T = fp8bs.requant_e5m6_to_128x1(e5[0], e5[1])
+    quant_row("Q3-E5M6 requant X cache 4096x2048 -> 128x1 E4M3",
+              lambda: fp8bs.requant_e5m6_to_128x1(e5[0], e5[1], qT=q5T, scalesT=s5T),
+              int(n_x * (1.5 + 1 + 8 / 128)))
+    del e5, q5T, s5T
     qdyT, sdyT = fp8bs.quant_act_1x128(dy, transpose_out=True)
     quant_row("Q1T dY 4096x7168 (128x1, transposed out)",
               lambda: fp8bs.quant_act_1x128(dy, transpose_out=True, q=qdyT, scales=sdyT),

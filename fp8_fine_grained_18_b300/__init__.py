@@ -40,6 +40,8 @@ _SIGS = {
     "fp8bs_quant_act_1x128": [_P, _I64, _I64, _I, _P, _P, _P],
     "fp8bs_quant_weight_128x128": [_P, _I64, _I64, _P, _P, _P, _P, _P],
     "fp8bs_quant_act_dual": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "fp8bs_quant_act_e5m6": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "fp8bs_requant_e5m6_to_128x1": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8bs_quant_per_tensor": [_P, _I64, _I64, _P, _P, _P, _I64, _P],
     "fp8bs_requant_1x128_to_128x1": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8bs_gemm": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P],
@@ -139,6 +141,38 @@ def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, q=None, scal
                                            _ptr(scalesT if transposed else None), _stream(w)),
            "fp8bs_quant_weight_128x128")
     return (q, scales, qT, scalesT) if transposed else (q, scales)
+
+
+def quant_act_e5m6(x: torch.Tensor, with_e4m3: bool = True, packed=None, scales=None, q=None,
+                   q_scales=None):
+    """E5M6 cache of x bf16 [M, K] with 1x128 scales, plus (with_e4m3) the
+    E4M3 1x128 codes from the same read.
+
+    Returns (packed uint8 [M, 3K/2], scales float32 [K/128, M], q, q_scales);
+    q and q_scales are None without with_e4m3."""
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    M, K = x.shape
+    packed = _empty((M, K // 2 * 3), torch.uint8, x) if packed is None else packed
+    scales = _empty((K // GROUP, M), torch.float32, x) if scales is None else scales
+    if with_e4m3:
+        q = _empty((M, K), torch.uint8, x) if q is None else q
+        q_scales = _empty((K // GROUP, M), torch.float32, x) if q_scales is None else q_scales
+    else:
+        q = q_scales = None
+    _check(_lib.fp8bs_quant_act_e5m6(_ptr(x), M, K, _ptr(packed), _ptr(scales), _ptr(q),
+                                     _ptr(q_scales), _stream(x)), "fp8bs_quant_act_e5m6")
+    return packed, scales, q, q_scales
+
+
+def requant_e5m6_to_128x1(packed: torch.Tensor, scales: torch.Tensor, qT=None, scalesT=None):
+    """E5M6 cache [M, 3K/2] + scales [K/128, M] -> (qT uint8 [K, M], scalesT [M/128, K])."""
+    M, K = packed.shape[0], packed.shape[1] // 3 * 2
+    qT = _empty((K, M), torch.uint8, packed) if qT is None else qT
+    scalesT = _empty((M // GROUP, K), torch.float32, packed) if scalesT is None else scalesT
+    _check(_lib.fp8bs_requant_e5m6_to_128x1(_ptr(packed), _ptr(scales), M, K, _ptr(qT),
+                                            _ptr(scalesT), _stream(packed)),
+           "fp8bs_requant_e5m6_to_128x1")
+    return qT, scalesT
 
 
 def quant_per_tensor(x: torch.Tensor, q=None, scale=None, bcast_shape=None, bcast=None):

@@ -163,6 +163,40 @@ fp8bs_status fp8bs_quant_per_tensor(const void* x_bf16, int64_t rows, int64_t co
                                                     n_bcast, as_cuda(stream)));
 }
 
+fp8bs_status fp8bs_quant_act_e5m6(const void* x_bf16, int64_t M, int64_t K, uint8_t* packed,
+                                  float* scales, uint8_t* q, float* q_scales,
+                                  fp8bs_stream_t stream) {
+  if (M < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if ((q == nullptr) != (q_scales == nullptr)) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (!x_bf16 || !packed || !scales) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (K / 128 > 65535 || M >= kMaxDim * 64) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(packed) || !aligned16(scales) || (q && !aligned16(q)) ||
+      (q_scales && !aligned16(q_scales)))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(
+      fp8bs::launch_quant_act_e5m6(x_bf16, M, K, packed, scales, q, q_scales, as_cuda(stream)));
+}
+
+fp8bs_status fp8bs_requant_e5m6_to_128x1(const uint8_t* packed, const float* scales, int64_t M,
+                                         int64_t K, uint8_t* qT, float* scalesT,
+                                         fp8bs_stream_t stream) {
+  if (M < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return FP8BS_OK;
+  if (!packed || !scales || !qT || !scalesT) return FP8BS_ERR_INVALID_ARG;
+  if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (M / 128 > 65535 || K / 128 > (int64_t)1 << 30) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(packed) || !aligned16(scales) || !aligned16(qT) || !aligned16(scalesT))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(
+      fp8bs::launch_requant_e5m6_to_128x1(packed, scales, M, K, qT, scalesT, as_cuda(stream)));
+}
+
 fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t* q, const float* scales, int64_t M,
                                           int64_t K, uint8_t* qT, float* scalesT,
                                           fp8bs_stream_t stream) {

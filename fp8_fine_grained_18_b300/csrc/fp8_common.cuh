@@ -20,6 +20,7 @@ namespace fp8bs {
 
 constexpr int kGroup = 128;          // 1x128 tiles, 128x128 blocks
 constexpr float kE4M3Max = 448.0f;   // largest finite E4M3FN value
+constexpr float kE5M6Max = 65024.0f;  // largest finite E5M6 value (1.984375 * 2^15)
 // Below this scale the reciprocal-based quotient can meet FP32 subnormals;
 // such groups take the exact-division path.
 constexpr float kFastScaleMin = 0x1.0p-92f;
@@ -45,8 +46,11 @@ __device__ __forceinline__ float2 e4m3x2_decode(uint32_t two_codes) {
   return make_float2(lo, hi);
 }
 
-// Scale of a group whose max magnitude is amax.
-__device__ __forceinline__ float group_scale(float amax) { return __fdiv_rn(amax, kE4M3Max); }
+// Scale of a group whose max magnitude is amax, for a format whose largest
+// finite value is fmt_max (448 for E4M3; 65024 for the E5M6 cache).
+__device__ __forceinline__ float group_scale(float amax, float fmt_max = kE4M3Max) {
+  return __fdiv_rn(amax, fmt_max);
+}
 
 // Fast path: a normal, finite scale s with nr = -fl32(1/s) (a correctly
 // rounded reciprocal, negated).  The quotient is formed negated, by one
@@ -111,9 +115,9 @@ struct GroupScale {
 // Scale of a group from its amax given as a bit pattern (bf16 when bf16 is
 // true, else FP32); special = the group holds Inf or NaN.
 __device__ __forceinline__ GroupScale make_scale(uint32_t mag_no_nan_bits, bool special,
-                                                 bool bf16) {
+                                                 bool bf16, float fmt_max = kE4M3Max) {
   GroupScale g;
-  g.s = group_scale(__uint_as_float(bf16 ? mag_no_nan_bits << 16 : mag_no_nan_bits));
+  g.s = group_scale(__uint_as_float(bf16 ? mag_no_nan_bits << 16 : mag_no_nan_bits), fmt_max);
   g.fast = !special && g.s >= kFastScaleMin;
   g.nr = g.fast ? -__frcp_rn(g.s) : 0.0f;
   return g;
@@ -129,6 +133,58 @@ __device__ __forceinline__ uint32_t codes_f32x4(float a, float b, float c, float
   }
   return e4m3x2_nan(quotient_general(a, g.s), quotient_general(b, g.s)) |
          (e4m3x2_nan(quotient_general(c, g.s), quotient_general(d, g.s)) << 16);
+}
+
+// ---------------------------------------------------------------------------
+// E5M6, the 12-bit cache format of the activations that are re-tiled from
+// 1x128 to 128x1 tiles (page P1, paragraph 3): sign, 5 exponent bits (bias
+// 15), 6 mantissa bits; exponent 0 holds the subnormals m * 2^-20, exponent
+// 31 Inf/NaN.  Rounding to nearest even, saturating at 65024; NaN -> 0x7FF.
+// Codes are stored as a little-endian 12-bit stream (element i at bits
+// 12i .. 12i+11 of its row).
+// ---------------------------------------------------------------------------
+
+// Code of the FP32 value with magnitude bits `a` (no sign bit) and sign
+// `sign12` (0 or 0x800).
+__device__ __forceinline__ uint32_t e5m6_code(uint32_t a, uint32_t sign12) {
+  if (a > 0x7F800000u) return 0x7FFu;                      // NaN
+  if (a >= 0x477E0000u) return sign12 | 0x7BFu;            // >= 65024 (and Inf): saturate
+  if (a < 0x38800000u)                                     // below 2^-14: subnormal
+    return sign12 | __float2uint_rn(__uint_as_float(a) * 0x1.0p20f);  // exact scaling; 64 = 2^-14
+  // normal: round the FP32 significand to 6 bits, ties to even; a carry
+  // moves into the exponent field, and nothing below 65024 rounds past it
+  const uint32_t r = (a + 0xFFFFu + ((a >> 17) & 1u)) & ~0x1FFFFu;
+  return sign12 | (((r >> 23) - 112u) << 6) | ((r >> 17) & 0x3Fu);
+}
+
+// Code of y, and of -Q for a negated quotient Q (see neg_quotient_1step_x2).
+__device__ __forceinline__ uint32_t e5m6_of(float y) {
+  const uint32_t u = __float_as_uint(y);
+  return e5m6_code(u & 0x7FFFFFFFu, (u >> 20) & 0x800u);
+}
+__device__ __forceinline__ uint32_t e5m6_of_neg(float q) {
+  const uint32_t u = __float_as_uint(q);
+  return e5m6_code(u & 0x7FFFFFFFu, (~u >> 20) & 0x800u);
+}
+
+// Exact value of a code.
+__device__ __forceinline__ float e5m6_decode(uint32_t c) {
+  const uint32_t e = (c >> 6) & 0x1Fu, m = c & 0x3Fu;
+  float v;
+  if (e == 0u)
+    v = (float)m * 0x1.0p-20f;
+  else if (e == 31u)
+    v = __uint_as_float(m ? 0x7FC00000u : 0x7F800000u);
+  else
+    v = __uint_as_float(((e + 112u) << 23) | (m << 17));
+  return __uint_as_float(__float_as_uint(v) | ((c & 0x800u) << 20));
+}
+
+// Eight codes -> the 96-bit little-endian stream, as three words.
+__device__ __forceinline__ uint3 e5m6_pack8(const uint32_t* c) {
+  return make_uint3(c[0] | (c[1] << 12) | (c[2] << 24),
+                    (c[2] >> 8) | (c[3] << 4) | (c[4] << 16) | (c[5] << 28),
+                    (c[5] >> 4) | (c[6] << 8) | (c[7] << 20));
 }
 
 }  // namespace fp8bs

@@ -26,6 +26,13 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uin
 // n_bcast copies of the scale in bcast (nullable when n_bcast == 0).
 cudaError_t launch_quant_per_tensor(const void* x, int64_t n, uint8_t* q, float* scale,
                                     float* bcast, int64_t n_bcast, cudaStream_t stream);
+// E5M6 cache (packed [M][3K/2], scales [K/128][M]) of a bf16 activation,
+// with its E4M3 1x128 codes from the same read when q is non-null.
+cudaError_t launch_quant_act_e5m6(const void* x, int64_t M, int64_t K, uint8_t* e5, float* s5,
+                                  uint8_t* q, float* s, cudaStream_t stream);
+// The E5M6 cache re-tiled to 128x1 E4M3 tiles, transposed (M % 128 == 0).
+cudaError_t launch_requant_e5m6_to_128x1(const uint8_t* e5, const float* s5, int64_t M, int64_t K,
+                                         uint8_t* qT, float* sT, cudaStream_t stream);
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                           uint8_t* qT, float* sT, cudaStream_t stream);
 

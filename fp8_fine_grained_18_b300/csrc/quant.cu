@@ -124,6 +124,51 @@ struct Team {
   uint64_t* empty;   // empty barrier of the stage being consumed
 };
 
+// Q1's per-row maxima: half-warp rows h, h+32, h+64, h+96, eight bf16 of
+// each per lane (v[i] for row i).  Returns in lane j (0..3) of the half-warp
+// row j's NaN-free max magnitude (mj) and its plain max (pj >= Inf flags a
+// group with Inf or NaN), both as bf16 bit patterns.
+__device__ __forceinline__ void q1_row_max(const uint4* v, int l16, uint32_t& mj, uint32_t& pj) {
+  // per-row maxima, two rows packed per word, reduced over the half-warp
+  uint32_t m01 = 0, m23 = 0;
+  {
+    uint32_t a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      a[i] = halves_max(mag_pair_max(mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y),
+                                                  v[i].z),
+                                     v[i].w));
+    m01 = a[0] | (a[1] << 16);
+    m23 = a[2] | (a[3] << 16);
+  }
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) {
+    m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
+    m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
+  }
+  const uint32_t plain01 = m01, plain23 = m23;
+  if (__any_sync(kFull, pair_has_nan(m01) || pair_has_nan(m23))) {  // recount without NaN
+    uint32_t a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      a[i] = halves_max(mag_pair_max_no_nan(
+          mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
+                              v[i].z),
+          v[i].w));
+    m01 = a[0] | (a[1] << 16);
+    m23 = a[2] | (a[3] << 16);
+#pragma unroll
+    for (int off = 8; off >= 1; off >>= 1) {
+      m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
+      m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
+    }
+  }
+  const int j = l16 & 3;
+  const uint32_t mw = j < 2 ? m01 : m23, pw = j < 2 ? plain01 : plain23;
+  mj = (j & 1) ? (mw >> 16) : (mw & 0xFFFFu);
+  pj = (j & 1) ? (pw >> 16) : (pw & 0xFFFFu);
+}
+
 // ---------------------------------------------------------------------------
 // Q1: 1x128 tiles.  Tile = 128 rows x one K-group (TMA box 128 x 128 bf16,
 // 32 KB).  Half-warp h (0..31) owns rows h, h + 32, h + 64, h + 96 of the
@@ -157,46 +202,9 @@ struct Q1 {
     uint4 v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = st[(hw + 32 * i) * 16 + l16];
-    // per-row maxima, two rows packed per word, reduced over the half-warp
-    uint32_t m01 = 0, m23 = 0;
-    {
-      uint32_t a[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        a[i] = halves_max(mag_pair_max(mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y),
-                                                    v[i].z),
-                                       v[i].w));
-      m01 = a[0] | (a[1] << 16);
-      m23 = a[2] | (a[3] << 16);
-    }
-#pragma unroll
-    for (int off = 8; off >= 1; off >>= 1) {
-      m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
-      m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
-    }
-    const uint32_t plain01 = m01, plain23 = m23;
-    if (__any_sync(kFull, pair_has_nan(m01) || pair_has_nan(m23))) {  // recount without NaN
-      uint32_t a[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        a[i] = halves_max(mag_pair_max_no_nan(
-            mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
-                                v[i].z),
-            v[i].w));
-      m01 = a[0] | (a[1] << 16);
-      m23 = a[2] | (a[3] << 16);
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) {
-        m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
-        m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
-      }
-    }
+    uint32_t mj, pj;
+    q1_row_max(v, l16, mj, pj);
     release_stage(tm.empty, lane);
-    // lane j (0..3) of the half-warp computes row j's scale
-    const int j = l16 & 3;
-    const uint32_t mw = j < 2 ? m01 : m23, pw = j < 2 ? plain01 : plain23;
-    const uint32_t mj = (j & 1) ? (mw >> 16) : (mw & 0xFFFFu);
-    const uint32_t pj = (j & 1) ? (pw >> 16) : (pw & 0xFFFFu);
     const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
     const int64_t col = (int64_t)kb * kGroup + l16 * 8;
 #pragma unroll
@@ -206,6 +214,87 @@ struct Q1 {
       if (r < p.M) {
         *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[i], g);
         if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Q1E5: the E5M6 cache of an activation that will be re-tiled for the
+// weight gradient (page P1, paragraph 3), optionally with its E4M3 1x128
+// codes for the forward GEMM from the same read.  Same tiles and thread
+// layout as Q1; each lane writes its eight 12-bit codes as three words.
+// ---------------------------------------------------------------------------
+struct Q1E5 {
+  static constexpr int kRows = 128;
+  static constexpr int kStageBytes = kRows * 256;
+  static constexpr int kStages = 4;
+  static constexpr int kScratchBytes = 0;
+  static constexpr uint32_t kTx = kStageBytes;
+  static constexpr int kTeams = 1;
+  struct Params {
+    uint8_t* e5;  // [M][3K/2]
+    float* s5;    // [K/128][M]
+    uint8_t* q;   // E4M3 [M][K] or null
+    float* s;     // [K/128][M] or null
+    int M, K, KB, num_tiles;
+  };
+  __device__ static void issue(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile,
+                               const Params& p) {
+    ptx::tma_load_2d(dst, map, bar, (tile % p.KB) * kGroup, (tile / p.KB) * kRows);
+  }
+  __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
+                                 const Team& tm) {
+    const int kb = tile % p.KB, rt = tile / p.KB;
+    const int lane = tm.lane;
+    const int hw = tm.warp * 2 + (lane >> 4);
+    const int l16 = lane & 15;
+    const uint4* st = reinterpret_cast<const uint4*>(stage);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = st[(hw + 32 * i) * 16 + l16];
+    uint32_t mj, pj;
+    q1_row_max(v, l16, mj, pj);
+    release_stage(tm.empty, lane);
+    const GroupScale mine5 = make_scale(mj, pj >= kBf16Inf, true, kE5M6Max);
+    const GroupScale mine8 = make_scale(mj, pj >= kBf16Inf, true);
+    const int64_t col = (int64_t)kb * kGroup + l16 * 8;
+    const int64_t row_bytes = (int64_t)p.K / 2 * 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const GroupScale g5 = shfl_scale(mine5, (lane & 16) + i);
+      const int64_t r = (int64_t)rt * kRows + hw + 32 * i;
+      uint32_t c[8];
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      if (g5.fast) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 qn =
+              neg_quotient_1step_x2(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), g5.s, g5.nr);
+          c[2 * k] = e5m6_of_neg(qn.x);
+          c[2 * k + 1] = e5m6_of_neg(qn.y);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          c[2 * k] = e5m6_of(quotient_general(bf16_lo(w[k]), g5.s));
+          c[2 * k + 1] = e5m6_of(quotient_general(bf16_hi(w[k]), g5.s));
+        }
+      }
+      if (p.q) {
+        const GroupScale g8 = shfl_scale(mine8, (lane & 16) + i);
+        if (r < p.M) {
+          *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[i], g8);
+          if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine8.s;
+        }
+      }
+      if (r < p.M) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(p.e5 + r * row_bytes + col / 2 * 3);
+        const uint3 pk = e5m6_pack8(c);
+        dst[0] = pk.x;
+        dst[1] = pk.y;
+        dst[2] = pk.z;
+        if (l16 == i) p.s5[(int64_t)kb * p.M + r] = mine5.s;
       }
     }
   }
@@ -633,36 +722,67 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, float (&o)[4]) {
   o[3] = b.y;
 }
 
+// Four E5M6 codes of one row (row r of a 128-column tile staged as its
+// 192-byte packed stream; columns 4 cq .. 4 cq + 3 are bytes 6 cq .. 6 cq + 5),
+// dequantized with that row's scale: one round-to-nearest multiply each.
+__device__ __forceinline__ void dequant4_e5m6(const uint16_t* t16, int r, int cq, float s,
+                                              float (&o)[4]) {
+  const int h = r * 96 + 3 * cq;
+  const uint64_t w = (uint64_t)t16[h] | ((uint64_t)t16[h + 1] << 16) | ((uint64_t)t16[h + 2] << 32);
+  const float2 s2 = make_float2(s, s);
+  const float2 a = ptx::mul2_rn(make_float2(e5m6_decode((uint32_t)w & 0xFFFu),
+                                            e5m6_decode((uint32_t)(w >> 12) & 0xFFFu)), s2);
+  const float2 b = ptx::mul2_rn(make_float2(e5m6_decode((uint32_t)(w >> 24) & 0xFFFu),
+                                            e5m6_decode((uint32_t)(w >> 36) & 0xFFFu)), s2);
+  o[0] = a.x;
+  o[1] = a.y;
+  o[2] = b.x;
+  o[3] = b.y;
+}
+
 // Q3: 1x128 -> 128x1.  CTA tile = 128 rows (one 128-token group) x 128
 // columns (one K-group) of codes plus their 128 row scales.  Thread
 // (cq, part): columns 4 cq .. 4 cq + 3, rows 16 part .. 16 part + 15; the
 // values are dequantized once for the column maxima (float maxima that
 // propagate NaN; a column holding a NaN recounts without it) and again for
 // the codes.  grid = (K/128, M/128).
+// With E5 the input is the packed E5M6 cache ([M][3K/2] bytes, 1x128 scales
+// for a maximum of 65024) instead of E4M3 codes.
+template <bool E5>
 __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
     const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t M, int64_t K,
     uint8_t* __restrict__ qT, float* __restrict__ sT) {
-  __shared__ uint4 tile[128 * 8];  // row r, 16-byte segment g at [r * 8 + g]
+  constexpr int kSeg = E5 ? 12 : 8;  // 16-byte segments per tile row
+  __shared__ uint4 tile[128 * kSeg];  // row r, segment g at [r * kSeg + g]
   __shared__ float srow[128];
   __shared__ float red[8][128];
   const int t = threadIdx.x;
   const int64_t kb = blockIdx.x, mb = blockIdx.y;
   const int64_t k0 = kb * kGroup, m0 = mb * kGroup;
+  const int64_t row_bytes = E5 ? K / 2 * 3 : K;
+  const int64_t col_byte = E5 ? kb * 192 : k0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < kSeg / 2; ++j) {
     const int idx = t + 256 * j;
-    tile[idx] = ld_stream_v4(q + (m0 + (idx >> 3)) * K + k0 + (idx & 7) * 16);
+    tile[idx] = ld_stream_v4(q + (m0 + idx / kSeg) * row_bytes + col_byte + (idx % kSeg) * 16);
   }
   if (t < 128) srow[t] = s[kb * M + m0 + t];
   __syncthreads();
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
+  const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
   const int cq = t & 31, part = t >> 5;
+  auto dq = [&](int r, float (&xv)[4]) {
+    if constexpr (E5)
+      dequant4_e5m6(t16, r, cq, srow[r], xv);
+    else
+      dequant4(tw[r * 32 + cq], srow[r], xv);
+  };
   float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
   for (int i = 0; i < 16; ++i) {
     const int r = part * 16 + i;
     float xv[4];
-    dequant4(tw[r * 32 + cq], srow[r], xv);
+    dq(r, xv);
 #pragma unroll
     for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xv[c]);
   }
@@ -679,7 +799,7 @@ __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
       mn = 0.0f;
       for (int r = 0; r < 128; ++r) {
         float xv[4];
-        dequant4(tw[r * 32 + cq], srow[r], xv);
+        dq(r, xv);
         mn = fmaxf(mn, fabsf(xv[c]));
       }
     }
@@ -690,10 +810,10 @@ __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
   for (int i = 0; i < 16; i += 4) {
     const int r = part * 16 + i;
     float x0[4], x1[4], x2[4], x3[4];
-    dequant4(tw[r * 32 + cq], srow[r], x0);
-    dequant4(tw[(r + 1) * 32 + cq], srow[r + 1], x1);
-    dequant4(tw[(r + 2) * 32 + cq], srow[r + 2], x2);
-    dequant4(tw[(r + 3) * 32 + cq], srow[r + 3], x3);
+    dq(r, x0);
+    dq(r + 1, x1);
+    dq(r + 2, x2);
+    dq(r + 3, x3);
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
   }
@@ -779,7 +899,7 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uin
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                           uint8_t* qT, float* sT, cudaStream_t stream) {
   dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
-  requant_1x128_to_128x1_kernel<<<grid, 256, 0, stream>>>(q, s, M, K, qT, sT);
+  requant_1x128_to_128x1_kernel<false><<<grid, 256, 0, stream>>>(q, s, M, K, qT, sT);
   return cudaGetLastError();
 }
 
@@ -799,6 +919,29 @@ cudaError_t launch_quant_per_tensor(const void* x, int64_t n, uint8_t* q, float*
   tensor_quant_kernel<<<(unsigned)g2, kPtThreads, 0, stream>>>(
       xv, nvec, reinterpret_cast<uint2*>(q), scale, bcast, n_bcast);
   tensor_scale_finalize_kernel<<<1, 32, 0, stream>>>(scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_e5m6(const void* x, int64_t M, int64_t K, uint8_t* e5, float* s5,
+                                  uint8_t* q, float* s, cudaStream_t stream) {
+  CUtensorMap map;
+  if (!make_tmap_2d(&map, x, 2, M, K, kGroup, Q1E5::kRows, false)) return cudaErrorInvalidValue;
+  Q1E5::Params p;
+  p.e5 = e5;
+  p.s5 = s5;
+  p.q = q;
+  p.s = s;
+  p.M = (int)M;
+  p.K = (int)K;
+  p.KB = (int)(K / kGroup);
+  p.num_tiles = (int)((M + Q1E5::kRows - 1) / Q1E5::kRows) * p.KB;
+  return launch_stream<Q1E5>(map, p, stream);
+}
+
+cudaError_t launch_requant_e5m6_to_128x1(const uint8_t* e5, const float* s5, int64_t M, int64_t K,
+                                         uint8_t* qT, float* sT, cudaStream_t stream) {
+  dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
+  requant_1x128_to_128x1_kernel<true><<<grid, 256, 0, stream>>>(e5, s5, M, K, qT, sT);
   return cudaGetLastError();
 }
 

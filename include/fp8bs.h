@@ -217,6 +217,41 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *a, const float *sa,
                               fp8bs_stream_t stream);
 
 /*
+ * E5M6 cache of an activation that the backward pass re-tiles from 1x128 to
+ * 128x1 tiles [P1¶3: a custom E5M6 format is used only for these
+ * activations].  Readings where the page is silent: E5M6 = sign, 5 exponent
+ * bits (bias 15), 6 mantissa bits, exponent 0 = subnormals m * 2^-20,
+ * exponent 31 = Inf/NaN, largest finite 65024 (code 0x7BF); rounding to
+ * nearest even, saturating; NaN -> 0x7FF.  The cache keeps 1x128 tiles:
+ * s = fl32(amax / 65024), code = E5M6(fl32(x / s)) (the rule of
+ * fp8bs_quant_act_1x128 with 65024 in place of 448).  Codes are packed as a
+ * little-endian 12-bit stream: element k of row m is bits 12k .. 12k+11 of
+ * the row's 3K/2 bytes.
+ *   x: bf16 [M][K] -> packed: [M][3K/2] bytes, scales: f32 [K/128][M].
+ *   q, q_scales (both null or both set): also the E4M3 1x128 codes and
+ *   scales of fp8bs_quant_act_1x128 for the forward GEMM, from the same read.
+ *   Requires K % 128 == 0; pointers 16-byte aligned.  M == 0 or K == 0 is
+ *   a no-op.
+ */
+fp8bs_status fp8bs_quant_act_e5m6(const void *x_bf16, int64_t M, int64_t K,
+                                  uint8_t *packed, float *scales, uint8_t *q,
+                                  float *q_scales, fp8bs_stream_t stream);
+
+/*
+ * The E5M6 cache re-tiled for the weight-gradient GEMM [P1¶3]: each element
+ * is dequantized with one round-to-nearest multiply, x^ = fl32(decode(code)
+ * * s), and the 128x1 rule of fp8bs_quant_act_1x128(transpose_out = 1) is
+ * applied to x^.
+ *   packed: [M][3K/2], scales: f32 [K/128][M] (fp8bs_quant_act_e5m6's
+ *   output) -> qT: E4M3 [K][M], scalesT: f32 [M/128][K].
+ *   Requires M % 128 == 0 and K % 128 == 0; pointers 16-byte aligned.
+ */
+fp8bs_status fp8bs_requant_e5m6_to_128x1(const uint8_t *packed,
+                                         const float *scales, int64_t M,
+                                         int64_t K, uint8_t *qT, float *scalesT,
+                                         fp8bs_stream_t stream);
+
+/*
  * Per-tensor FP8 quantization: the standard practice that the fine-grained
  * tiles replace [P1¶4][P3¶4] (one scale for the whole tensor, its max-abs
  * mapped to the FP8 maximum; sensitive to outliers).  Kept as the accuracy
