@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on (sha of gemm.cu, ptx.cuh,
 # fp8_common.cuh); reported as null once the source has changed.
-TRAFFIC = {"gemm": {"bytes": 86919424 + 35751168, "src_sha": "a985ce3c1daf6a2c"}}
+TRAFFIC = {"gemm": {"bytes": 87637760 + 35574016, "src_sha": "11c8df28b8b976db"}}
 
 
 def kernel_source_sha():
@@ -233,8 +233,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        fp8bs.quant_act_1x128(a, q=qa, scales=sa)
-        fp8bs.quant_weight_128x128(b, q=qb, scales=sb)
+        fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb)
         fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=c)
 
     for _ in range(args.warmup):
@@ -243,7 +242,7 @@ def run_ours(args):
     if fp8bs.get_device_error(dev) != fp8bs.OK:
         raise RuntimeError("device error during warm-up")
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -254,22 +253,19 @@ def run_ours(args):
             flush.zero_()
             e = ev[i]
             e[0].record(stream)
-            fp8bs.quant_act_1x128(a, q=qa, scales=sa)
+            fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb)
             e[1].record(stream)
-            fp8bs.quant_weight_128x128(b, q=qb, scales=sb)
-            e[2].record(stream)
             fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=c)
-            e[3].record(stream)
+            e[2].record(stream)
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     if world > 1:
         dist.barrier()
     if fp8bs.get_device_error(dev) != fp8bs.OK:
         raise RuntimeError("device error in the timed region")
-    t_q1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    t_q2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    t_g = [ev[i][2].elapsed_time(ev[i][3]) for i in range(args.steps)]
-    t_step = [ev[i][0].elapsed_time(ev[i][3]) for i in range(args.steps)]
+    t_q = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    t_g = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    t_step = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
     total_ms = max_over_ranks(sum(t_step), dist, dev)
     flops = 2.0 * M * N * K
     value = whole_job_rate(flops, world, args.steps, total_ms) / 1e12
@@ -291,13 +287,12 @@ def run_ours(args):
                 "frac_of_sustained": round(g_tflops / (peaks["bf16_tflops_sustained"] * FP8_OVER_BF16), 4),
                 "algorithmic_flops_per_launch": flops}
     hbm = peaks["hbm_gbs"]
-    q1_gbs = algorithmic_bytes_q1(M, K) / (statistics.mean(t_q1) * 1e-3) / 1e9
-    q2_gbs = algorithmic_bytes_q2(N, K) / (statistics.mean(t_q2) * 1e-3) / 1e9
+    q_gbs = (algorithmic_bytes_q1(M, K) + algorithmic_bytes_q2(N, K)) / \
+        (statistics.mean(t_q) * 1e-3) / 1e9
     kernels = {
-        "quant_act_1x128": {"ms": round(statistics.mean(t_q1), 4), "GB/s": round(q1_gbs, 1),
-                            "frac_hbm": round(q1_gbs / hbm, 4)},
-        "quant_weight_128x128": {"ms": round(statistics.mean(t_q2), 4), "GB/s": round(q2_gbs, 1),
-                                 "frac_hbm": round(q2_gbs / hbm, 4)},
+        "quant_act_and_weight (Q1 of A and Q2 of W, one launch)": {
+            "ms": round(statistics.mean(t_q), 4), "GB/s": round(q_gbs, 1),
+            "frac_hbm": round(q_gbs / hbm, 4)},
         "gemm": {"ms": round(g_ms, 4), "TFLOP/s": round(g_tflops, 1),
                  "frac_fp8_peak": round(g_tflops / fp8_peak, 4)},
     }
@@ -322,7 +317,7 @@ def run_ours(args):
                    "l2": "flushed between steps (256 MB write, outside the timed events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "kernels": kernels, "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(), "wall_timed_s": round(wall, 4),
     }
     if args.rows and rank == 0:
@@ -373,8 +368,8 @@ def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
                 comp.wait_event(loaded[k])
                 if read[k] is not None:
                     comp.wait_event(read[k])  # step i-2's result has been read back
-                fp8bs.quant_act_1x128(st["a"], q=st["qa"], scales=st["sa"])
-                fp8bs.quant_weight_128x128(st["b"], q=st["qb"], scales=st["sb"])
+                fp8bs.quant_act_and_weight(st["a"], st["b"], q=st["qa"], scales=st["sa"],
+                                           qw=st["qb"], w_scales=st["sb"])
                 fp8bs.gemm(st["qa"], st["sa"], st["qb"], st["sb"], fp8bs.BSCALE_BLOCK_128x128,
                            out_dtype=torch.bfloat16, out=st["c"])
                 done[k] = ev(); done[k].record(comp)
@@ -454,6 +449,18 @@ def measure_rows(fp8bs, torch, dev, peaks):
         ms = _time_ms(fn, torch, flush=flush)
         gbs = nbytes / (ms * 1e-3) / 1e9
         rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+
+    # the dense step's quantizers as separate launches
+    dense = synth.make_inputs("dense")
+    a, b = bf(dense["A"]), bf(dense["B"])
+    del dense
+    qa, sa = fp8bs.quant_act_1x128(a)
+    qb, sb = fp8bs.quant_weight_128x128(b)
+    quant_row("Q1 dense A 4096x7168 (own launch)", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
+              algorithmic_bytes_q1(4096, 7168))
+    quant_row("Q2 dense W 7168x7168 (own launch)",
+              lambda: fp8bs.quant_weight_128x128(b, q=qb, scales=sb), algorithmic_bytes_q2(7168, 7168))
+    del a, b, qa, sa, qb, sb
 
     # MoE up/gate shape
     moe = synth.make_inputs("moe")

@@ -40,6 +40,7 @@ _SIGS = {
     "fp8bs_quant_act_1x128": [_P, _I64, _I64, _I, _P, _P, _P],
     "fp8bs_quant_weight_128x128": [_P, _I64, _I64, _P, _P, _P, _P, _P],
     "fp8bs_quant_act_dual": [_P, _I64, _I64, _P, _P, _P, _P, _P],
+    "fp8bs_quant_act_and_weight": [_P, _I64, _I64, _P, _P, _P, _I64, _I64, _P, _P, _P],
     "fp8bs_quant_act_e5m6": [_P, _I64, _I64, _P, _P, _P, _P, _P],
     "fp8bs_requant_e5m6_to_128x1": [_P, _P, _I64, _I64, _P, _P, _P],
     "fp8bs_quant_per_tensor": [_P, _I64, _I64, _P, _P, _P, _I64, _P],
@@ -141,6 +142,26 @@ def quant_weight_128x128(w: torch.Tensor, transposed: bool = False, q=None, scal
                                            _ptr(scalesT if transposed else None), _stream(w)),
            "fp8bs_quant_weight_128x128")
     return (q, scales, qT, scalesT) if transposed else (q, scales)
+
+
+def quant_act_and_weight(x: torch.Tensor, w: torch.Tensor, q=None, scales=None, qw=None,
+                         w_scales=None):
+    """Q1 of x bf16 [M, K] and Q2 of w bf16 [N, Kw] in one launch.
+
+    Returns (q, scales, qw, w_scales) as quant_act_1x128 and
+    quant_weight_128x128 would."""
+    assert x.dtype == torch.bfloat16 and w.dtype == torch.bfloat16
+    assert x.is_contiguous() and w.is_contiguous()
+    M, K = x.shape
+    N, Kw = w.shape
+    q = _empty((M, K), torch.uint8, x) if q is None else q
+    scales = _empty((K // GROUP, M), torch.float32, x) if scales is None else scales
+    qw = _empty((N, Kw), torch.uint8, w) if qw is None else qw
+    w_scales = _empty((N // GROUP, Kw // GROUP), torch.float32, w) if w_scales is None else w_scales
+    _check(_lib.fp8bs_quant_act_and_weight(_ptr(x), M, K, _ptr(q), _ptr(scales), _ptr(w), N, Kw,
+                                           _ptr(qw), _ptr(w_scales), _stream(x)),
+           "fp8bs_quant_act_and_weight")
+    return q, scales, qw, w_scales
 
 
 def quant_act_e5m6(x: torch.Tensor, with_e4m3: bool = True, packed=None, scales=None, q=None,

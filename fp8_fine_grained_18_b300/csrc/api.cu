@@ -197,6 +197,27 @@ fp8bs_status fp8bs_requant_e5m6_to_128x1(const uint8_t* packed, const float* sca
       fp8bs::launch_requant_e5m6_to_128x1(packed, scales, M, K, qT, scalesT, as_cuda(stream)));
 }
 
+fp8bs_status fp8bs_quant_act_and_weight(const void* x_bf16, int64_t M, int64_t K, uint8_t* q,
+                                        float* scales, const void* w_bf16, int64_t N, int64_t Kw,
+                                        uint8_t* qw, float* w_scales, fp8bs_stream_t stream) {
+  if (M < 0 || K < 0 || N < 0 || Kw < 0) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || K == 0)
+    return fp8bs_quant_weight_128x128(w_bf16, N, Kw, qw, w_scales, nullptr, nullptr, stream);
+  if (N == 0 || Kw == 0) return fp8bs_quant_act_1x128(x_bf16, M, K, 0, q, scales, stream);
+  if (!x_bf16 || !q || !scales || !w_bf16 || !qw || !w_scales) return FP8BS_ERR_INVALID_ARG;
+  if (K % 128 != 0 || N % 128 != 0 || Kw % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  const int64_t tiles = ((M + 127) / 128) * (K / 128) + (N / 128) * (Kw / 128);
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim || Kw >= kMaxDim || tiles >= kMaxDim)
+    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales) || !aligned16(w_bf16) ||
+      !aligned16(qw) || !aligned16(w_scales))
+    return FP8BS_ERR_MISALIGNED;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  return cuda_status(fp8bs::launch_quant_act_and_weight(x_bf16, M, K, q, scales, w_bf16, N, Kw,
+                                                        qw, w_scales, as_cuda(stream)));
+}
+
 fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t* q, const float* scales, int64_t M,
                                           int64_t K, uint8_t* qT, float* scalesT,
                                           fp8bs_stream_t stream) {

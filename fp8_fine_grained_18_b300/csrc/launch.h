@@ -20,6 +20,11 @@ cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t*
                                    cudaStream_t stream);
 cudaError_t launch_quant_act_dual(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
                                   uint8_t* qT, float* sT, cudaStream_t stream);
+// Q1 of x [M][K] and Q2 of w [N][Kw] in one launch (same outputs as the two
+// launchers above).
+cudaError_t launch_quant_act_and_weight(const void* x, int64_t M, int64_t K, uint8_t* q,
+                                        float* s, const void* w, int64_t N, int64_t Kw,
+                                        uint8_t* qw, float* sw, cudaStream_t stream);
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,
                                         uint8_t* qT, float* sT, cudaStream_t stream);
 // Per-tensor scale of n bf16 values (n % 8 == 0): q codes, *scale, and

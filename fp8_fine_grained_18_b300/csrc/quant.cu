@@ -192,28 +192,36 @@ struct Q1 {
                                const Params& p) {
     ptx::tma_load_2d(dst, map, bar, (tile % p.KB) * kGroup, (tile / p.KB) * kRows);
   }
+  // R rows per half-warp: 4 when all 16 consumer warps share a tile, 8 for
+  // a team of 8 warps (the fused activation + weight launch).
+  template <int R = 4>
   __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
                                  const Team& tm) {
+    constexpr int kHalfWarps = kRows / R;
     const int kb = tile % p.KB, rt = tile / p.KB;
     const int lane = tm.lane;
     const int hw = tm.warp * 2 + (lane >> 4);
     const int l16 = lane & 15;
     const uint4* st = reinterpret_cast<const uint4*>(stage);
-    uint4 v[4];
+    uint4 v[R];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = st[(hw + 32 * i) * 16 + l16];
-    uint32_t mj, pj;
-    q1_row_max(v, l16, mj, pj);
+    for (int i = 0; i < R; ++i) v[i] = st[(hw + kHalfWarps * i) * 16 + l16];
+    uint32_t mj[R / 4], pj[R / 4];
+#pragma unroll
+    for (int b = 0; b < R / 4; ++b) q1_row_max(v + 4 * b, l16, mj[b], pj[b]);
     release_stage(tm.empty, lane);
-    const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
     const int64_t col = (int64_t)kb * kGroup + l16 * 8;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const GroupScale g = shfl_scale(mine, (lane & 16) + i);
-      const int64_t r = (int64_t)rt * kRows + hw + 32 * i;
-      if (r < p.M) {
-        *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[i], g);
-        if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+    for (int b = 0; b < R / 4; ++b) {
+      const GroupScale mine = make_scale(mj[b], pj[b] >= kBf16Inf, true);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const GroupScale g = shfl_scale(mine, (lane & 16) + i);
+        const int64_t r = (int64_t)rt * kRows + hw + kHalfWarps * (4 * b + i);
+        if (r < p.M) {
+          *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[4 * b + i], g);
+          if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+        }
       }
     }
   }
@@ -424,7 +432,8 @@ struct StreamSmem {
 // i, i + grid, ...; its j-th tile goes to team j mod kTeams.
 template <class Op>
 __global__ void __launch_bounds__(kThreads, 1)
-    stream_kernel(const __grid_constant__ CUtensorMap map, const typename Op::Params p) {
+    stream_kernel(const __grid_constant__ CUtensorMap map,
+                  const __grid_constant__ typename Op::Params p) {
   using L = StreamSmem<Op>;
   constexpr int S = Op::kStages;
   constexpr int kTeamWarps = kConsumerWarps / Op::kTeams;
@@ -517,6 +526,44 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
                : "l"(p));
   return v;
 }
+
+// ---------------------------------------------------------------------------
+// Q12: both operands of the forward GEMM in one launch -- an activation's
+// 1x128 tiles (tiles 0 .. t1-1, through the kernel's tensor map) and a
+// weight's 128x128 blocks (tiles t1 .., through map_w).  Both tile kinds are
+// 128 x 128 bf16 (32 KB); two teams of 8 warps take alternate tiles, so a
+// team quantizes an activation tile with 8 rows per half-warp.  One launch
+// pays the launch, ramp and tail once for the two tensors.
+// ---------------------------------------------------------------------------
+struct Q12 {
+  static constexpr int kStageBytes = 128 * 256;
+  static constexpr int kStages = 4;
+  static constexpr int kScratchBytes = Q2::kScratchBytes;
+  static constexpr uint32_t kTx = kStageBytes;
+  static constexpr int kTeams = 2;
+  static_assert(Q1::kStageBytes == kStageBytes && Q2::kStageBytes == kStageBytes, "tile size");
+  static_assert(Q2::kTeams == kTeams && Q2::kTeamWarps == kConsumerWarps / kTeams, "teams");
+  struct Params {
+    CUtensorMap map_w;  // 64-byte aligned: first member
+    Q1::Params a;
+    Q2::Params w;
+    int t1, num_tiles;
+  };
+  __device__ static void issue(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile,
+                               const Params& p) {
+    if (tile < p.t1)
+      Q1::issue(map, dst, bar, tile, p.a);
+    else
+      Q2::issue(&p.map_w, dst, bar, tile - p.t1, p.w);
+  }
+  __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
+                                 const Team& tm) {
+    if (tile < p.t1)
+      Q1::consume<8>(stage, tile, p.a, tm);
+    else
+      Q2::consume(stage, tile - p.t1, p.w, tm);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // Per-tensor baseline: one scale for the whole tensor, from its max-abs
@@ -877,6 +924,34 @@ cudaError_t launch_quant_act_dual(const void* x, int64_t M, int64_t K, uint8_t* 
   quant_act_128x1_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
                                                           qT, sT, q, s);
   return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_and_weight(const void* x, int64_t M, int64_t K, uint8_t* q,
+                                        float* s, const void* w, int64_t N, int64_t Kw,
+                                        uint8_t* qw, float* sw, cudaStream_t stream) {
+  Q12::Params p;
+  CUtensorMap map_a;
+  if (!make_tmap_2d(&map_a, x, 2, M, K, kGroup, Q1::kRows, false)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&p.map_w, w, 2, N, Kw, kGroup, kGroup, false)) return cudaErrorInvalidValue;
+  p.a.q = q;
+  p.a.s = s;
+  p.a.M = (int)M;
+  p.a.K = (int)K;
+  p.a.KB = (int)(K / kGroup);
+  p.a.num_tiles = (int)((M + Q1::kRows - 1) / Q1::kRows) * p.a.KB;
+  p.a.unused = nullptr;
+  p.w.q = qw;
+  p.w.s = sw;
+  p.w.qT = nullptr;
+  p.w.sT = nullptr;
+  p.w.N = (int)N;
+  p.w.K = (int)Kw;
+  p.w.KB = (int)(Kw / kGroup);
+  p.w.NB = (int)(N / kGroup);
+  p.w.num_tiles = p.w.NB * p.w.KB;
+  p.t1 = p.a.num_tiles;
+  p.num_tiles = p.a.num_tiles + p.w.num_tiles;
+  return launch_stream<Q12>(map_a, p, stream);
 }
 
 cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uint8_t* q, float* s,

@@ -217,6 +217,23 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *a, const float *sa,
                               fp8bs_stream_t stream);
 
 /*
+ * Both operands of the forward GEMM quantized in one launch [P1¶3]: the
+ * activation x in 1x128 tiles (exactly fp8bs_quant_act_1x128 with
+ * transpose_out = 0) and the weight w in 128x128 blocks (exactly
+ * fp8bs_quant_weight_128x128 without the transposed copy).  One launch pays
+ * the launch, pipeline ramp and tail once for both tensors.
+ *   x: bf16 [M][K] -> q: E4M3 [M][K], scales: f32 [K/128][M];
+ *   w: bf16 [N][Kw] -> qw: E4M3 [N][Kw], w_scales: f32 [N/128][Kw/128].
+ *   Requires K, N, Kw % 128 == 0 (M any); pointers 16-byte aligned.  An
+ *   empty operand leaves the call to the other one.
+ */
+fp8bs_status fp8bs_quant_act_and_weight(const void *x_bf16, int64_t M,
+                                        int64_t K, uint8_t *q, float *scales,
+                                        const void *w_bf16, int64_t N,
+                                        int64_t Kw, uint8_t *qw,
+                                        float *w_scales, fp8bs_stream_t stream);
+
+/*
  * E5M6 cache of an activation that the backward pass re-tiles from 1x128 to
  * 128x1 tiles [P1¶3: a custom E5M6 format is used only for these
  * activations].  Readings where the page is silent: E5M6 = sign, 5 exponent

@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
                      "fp8bs_requant_1x128_to_128x1", "fp8bs_quant_act_dual", "fp8bs_gemm",
                      "fp8bs_gemm_ex", "fp8bs_gemm_quant_out", "fp8bs_quant_per_tensor",
                      "fp8bs_quant_act_e5m6", "fp8bs_requant_e5m6_to_128x1",
+                     "fp8bs_quant_act_and_weight",
                      "fp8bs_status_string", "fp8bs_get_device_error"):
         assert required in names
 
@@ -73,6 +74,15 @@ def test_quant_argument_errors(libfp8bs):
     assert L.fp8bs_quant_act_dual(FAKE, 100, 128, FAKE, FAKE, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_quant_act_dual(FAKE, 128, 128, FAKE_ODD, FAKE, FAKE, FAKE, None) == m.ERR_MISALIGNED
     assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 129, 128, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    aw = L.fp8bs_quant_act_and_weight
+    assert aw(None, 0, 128, None, None, None, 0, 128, None, None, None) == m.OK
+    assert aw(FAKE, -1, 128, FAKE, FAKE, FAKE, 128, 128, FAKE, FAKE, None) == m.ERR_INVALID_ARG
+    assert aw(FAKE, 4, 128, FAKE, FAKE, None, 128, 128, FAKE, FAKE, None) == m.ERR_INVALID_ARG
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE, 100, 128, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert aw(FAKE, 4, 96, FAKE, FAKE, FAKE, 128, 128, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert aw(FAKE, 4, 128, FAKE, FAKE, FAKE_ODD, 128, 128, FAKE, FAKE, None) == m.ERR_MISALIGNED
+    # an empty operand defers to the other call's checks
+    assert aw(FAKE, 0, 128, None, None, FAKE, 100, 128, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
     e5 = L.fp8bs_quant_act_e5m6
     assert e5(None, 0, 128, None, None, None, None, None) == m.OK
     assert e5(FAKE, 4, 128, FAKE, FAKE, FAKE, None, None) == m.ERR_INVALID_ARG  # q without scales

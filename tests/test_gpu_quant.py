@@ -238,3 +238,25 @@ def test_hand_worked_tiles_on_gpu(fp8bs):
     q = q.cpu().numpy()
     for i, (amax, x, code) in enumerate(rows):
         assert q[i, 1] == code, (amax, x, hex(q[i, 1]), hex(code))
+
+
+@pytest.mark.parametrize("M,K,N,Kw", [(1, 128, 128, 128), (300, 1024, 384, 1024),
+                                      (129, 256, 1024, 640), (4096, 7168, 7168, 7168)])
+def test_act_and_weight_one_launch(fp8bs, oracle_mod, M, K, N, Kw):
+    """Q1 and Q2 in one launch: every code and scale of both outputs equals
+    the oracle's (the last case is the dense projection workload)."""
+    if (M, K) == (4096, 7168):
+        inp = synth.make_inputs("dense")
+        a_bits, w_bits = inp["A"], inp["B"]
+    else:
+        rng = np.random.default_rng(M + N + K + Kw)
+        a_bits, _ = synth.normal_with_outlier_columns(rng, (M, K), 3, 100.0)
+        w_bits = synth.normal(rng, (N, Kw), 0.02)
+        w_bits[5 % N, 7] = synth.f32_to_bf16_bits(np.array([np.nan], np.float32))[0]
+    q, s, qw, sw = fp8bs.quant_act_and_weight(dev_bf16(a_bits), dev_bf16(w_bits))
+    q_ref, s_ref = oracle_mod.quant_act_1x128(a_bits)
+    qw_ref, sw_ref = oracle_mod.quant_weight_128x128(w_bits)
+    assert_codes_equal(q, q_ref, "activation codes")
+    assert_scales_equal(s, s_ref, "activation scales")
+    assert_codes_equal(qw, qw_ref, "weight codes")
+    assert_scales_equal(sw, sw_ref, "weight scales")
