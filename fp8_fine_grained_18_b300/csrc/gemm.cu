@@ -77,15 +77,26 @@ struct Params {
 
 // Bounded wait.  Returns false when this wait expired (the error word and
 // the CTA's abort flag get set) or another role already aborted.
+// With SUSPEND the waiting thread sleeps in the barrier (at most 20 us per
+// try, so the time limit below still holds) instead of polling.
+template <bool SUSPEND = false>
+__device__ __forceinline__ bool try_wait(uint32_t addr, uint32_t parity) {
+  if constexpr (SUSPEND)
+    return ptx::mbar_try_wait_suspend<20000>(addr, parity);
+  else
+    return ptx::mbar_try_wait(addr, parity);
+}
+
+template <bool SUSPEND = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned int site) {
   const uint32_t addr = ptx::smem_addr(bar);
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
-    if (ptx::mbar_try_wait(addr, parity)) return true;
+    if (try_wait<SUSPEND>(addr, parity)) return true;
   const uint64_t t0 = ptx::globaltimer();
   while (true) {
-    if (ptx::mbar_try_wait(addr, parity)) return true;
+    if (try_wait<SUSPEND>(addr, parity)) return true;
     if (*abort_flag) return false;
     if (ptx::globaltimer() - t0 > kTimeoutNs) {
       *abort_flag = 1;
@@ -267,6 +278,11 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   constexpr int kPromoWarps = L::kPromoWarps;
   constexpr int STAGES = L::kStages;
   constexpr int TBUF = L::kTBuf;
+  // The MMA issuer sleeps in its barrier waits for the 128 x 224 tile (the
+  // dense projection's shape): measured +5% there, where the issuer's
+  // polling competed with the promotion warps of its sub-partition; the
+  // 256-wide tiles measured the same or slower with it, so they poll.
+  constexpr bool kMmaSuspend = (BN == 224 && !PAIR && PW == 8);
   constexpr int kCols = L::kCols;  // columns per promotion warp
   constexpr uint32_t kTmemCols = 512;
   // a CTA pair runs M = 256 MMAs, each CTA holding 128 rows of A and of D
@@ -402,10 +418,16 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         if (PROMOTE) {
           for (int kb = 0; kb < KB; ++kb, ++it, ++kt) {
             const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
-            if (!wait_bar(&tempty[buf], tph ^ 1, abort_flag, kErrMma)) { ok = false; break; }
+            if (!wait_bar<kMmaSuspend>(&tempty[buf], tph ^ 1, abort_flag, kErrMma)) {
+              ok = false;
+              break;
+            }
             ptx::tc_fence_after();
             const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
-            if (!wait_bar(&full[stage], phase, abort_flag, kErrMma)) { ok = false; break; }
+            if (!wait_bar<kMmaSuspend>(&full[stage], phase, abort_flag, kErrMma)) {
+              ok = false;
+              break;
+            }
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);

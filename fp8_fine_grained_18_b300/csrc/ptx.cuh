@@ -58,6 +58,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
   return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete may be suspended
+// by the hardware until the phase completes (at most `hint_ns`) instead of
+// returning at once: a waiter that does not poll leaves issue slots and
+// shared-memory bandwidth to the warps it shares an SM sub-partition with.
+template <uint32_t hint_ns>
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity), "n"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---- TMA --------------------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
