@@ -278,11 +278,12 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   constexpr int kPromoWarps = L::kPromoWarps;
   constexpr int STAGES = L::kStages;
   constexpr int TBUF = L::kTBuf;
-  // The MMA issuer sleeps in its barrier waits for the 128 x 224 tile (the
-  // dense projection's shape): measured +5% there, where the issuer's
-  // polling competed with the promotion warps of its sub-partition; the
-  // 256-wide tiles measured the same or slower with it, so they poll.
-  constexpr bool kMmaSuspend = (BN == 224 && !PAIR && PW == 8);
+  // The MMA issuer sleeps in its barrier waits instead of polling on the
+  // one-CTA-per-tile shapes narrower than 256 with 8 promotion warps: there
+  // its polling competed with the promotion warps of its sub-partition, and
+  // sleeping measured +5% (128 x 224) to +16% (128 x 128).  The 256-wide,
+  // CTA-pair and 12-warp shapes measured the same either way and poll.
+  constexpr bool kMmaSuspend = !PAIR && PW == 8 && BN < 256;
   constexpr int kCols = L::kCols;  // columns per promotion warp
   constexpr uint32_t kTmemCols = 512;
   // a CTA pair runs M = 256 MMAs, each CTA holding 128 rows of A and of D
