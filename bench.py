@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on (sha of gemm.cu, ptx.cuh,
 # fp8_common.cuh); reported as null once the source has changed.
-TRAFFIC = {"gemm": {"bytes": 87637760 + 35574016, "src_sha": "11c8df28b8b976db"}}
+TRAFFIC = {"gemm": {"bytes": 86909696 + 35542528, "src_sha": "61aad7b1c97b9339"}}
 
 
 def kernel_source_sha():
@@ -115,26 +115,46 @@ class ClockSampler:
             self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
         elif self.mode == "smi":
+            import shutil
             import subprocess
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index),
-                 "--query-gpu=" + ",".join(self.SMI_FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            cmd = ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                   "--format=csv,noheader,nounits", "-lms", "10"]
+            if shutil.which("stdbuf"):
+                cmd = ["stdbuf", "-oL"] + cmd  # one line per sample, as it is taken
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True, bufsize=1)
+            self.lines = []
+            self.t = threading.Thread(target=self._read_smi, daemon=True)
+            self.t.start()
+            # the sampler must be running before the timed region starts
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 10.0:
+                time.sleep(0.005)
+        self.t_begin = time.perf_counter()
         return self
 
+    def _read_smi(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
+
     def __exit__(self, *a):
+        self.t_end = time.perf_counter()
         if self.mode == "nvml":
             self._stop.set()
             self.t.join()
         elif self.mode == "smi":
+            time.sleep(0.03)  # the sample that covers the region's last milliseconds
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:  # noqa: BLE001
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            for line in out.splitlines():
+            self.t.join(timeout=5)
+            # samples taken while the timed region ran (plus one sampling
+            # interval after it)
+            for ts, line in list(self.lines):
+                if not (self.t_begin <= ts <= self.t_end + 0.02):
+                    continue
                 parts = [x.strip() for x in line.split(",")]
                 if len(parts) != 3:
                     continue
@@ -152,7 +172,7 @@ class ClockSampler:
         out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
                "samples": len(self.samples),
-               "source": {"nvml": "NVML, 5 ms polling", "smi": "nvidia-smi -lms 50",
+               "source": {"nvml": "NVML, 5 ms polling", "smi": "nvidia-smi -lms 10 (samples inside the timed region)",
                           None: "unavailable"}[self.mode]}
         if self.err and not self.samples:
             out["error"] = self.err
@@ -622,7 +642,7 @@ def _ref_step(oracle, inp, qw, sw, r0, rows, N, K):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", type=int, default=1, help="also time every hot-path row (1/0)")

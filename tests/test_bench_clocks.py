@@ -1,0 +1,64 @@
+"""The bench's clock sampler, on the CPU against a fake nvidia-smi: it must be
+sampling before the timed region starts, keep only the samples taken while
+the region ran, and report the throttle reasons it saw."""
+import os
+import stat
+import sys
+import time
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+FAKE = """#!/bin/sh
+# prints one sample line every 10 ms: SM MHz, max MHz, event-reason bits
+i=0
+while true; do
+  if [ -f "$FAKE_SMI_FLAG" ]; then echo "1500, 2032, 0x0000000000000004"; else echo "2032, 2032, 0x0000000000000000"; fi
+  i=$((i+1))
+  sleep 0.01
+done
+"""
+
+
+@pytest.fixture
+def fake_smi(tmp_path, monkeypatch):
+    exe = tmp_path / "nvidia-smi"
+    exe.write_text(FAKE)
+    exe.chmod(exe.stat().st_mode | stat.S_IEXEC)
+    flag = tmp_path / "capped"
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    monkeypatch.setenv("FAKE_SMI_FLAG", str(flag))
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench, flag
+
+
+def _sampler(bench):
+    s = bench.ClockSampler(0)
+    s.mode = "smi"  # no NVML on this host path
+    return s
+
+
+def test_sampler_records_region(fake_smi):
+    bench, _ = fake_smi
+    s = _sampler(bench)
+    with s:
+        assert s.lines, "sampling must have started before the region"
+        time.sleep(0.2)
+    out = s.summary()
+    assert out["samples"] >= 5
+    assert out["sm_mhz"] == 2032.0 and out["sm_max_mhz"] == 2032.0
+    assert out["reasons"] == []
+
+
+def test_sampler_reports_reasons_inside_region_only(fake_smi):
+    bench, flag = fake_smi
+    s = _sampler(bench)
+    with s:
+        flag.write_text("1")
+        time.sleep(0.2)
+    flag.unlink()
+    out = s.summary()
+    assert "sw_power_cap" in out["reasons"]
+    assert out["sm_mhz"] == 1500.0
