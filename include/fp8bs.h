@@ -13,7 +13,15 @@
  *     14 bits [P1¶3][P1¶4][P2¶3];
  *   - cached activations are re-tiled from 1x128 to 128x1 for the backward
  *     pass [P1¶3];
- *   - the GEMMs take FP8 inputs and write BF16 or FP32 [P4¶4].
+ *   - the GEMMs take FP8 inputs and write BF16 or FP32 [P4¶4];
+ *   - the activations that are re-tiled are kept in a custom E5M6 format
+ *     [P1¶3] (fp8bs_quant_act_e5m6, fp8bs_requant_e5m6_to_128x1);
+ *   - one scale per tensor is the standard practice that the tiles replace,
+ *     sensitive to outliers [P1¶4][P3¶4] (fp8bs_quant_per_tensor, kept as
+ *     the accuracy baseline);
+ *   - quantizing in a separate pass costs an HBM round trip [P2¶1]: the
+ *     fused calls (fp8bs_quant_act_and_weight, fp8bs_quant_act_dual,
+ *     fp8bs_gemm_quant_out) make several outputs from one read.
  * Page key: P1 = xn--9g3bo1gtkw0l8ubf92bgle.kr qna wr_id=32373,
  * P2 = why-be.why-be.co.kr as_center wr_id=73620,
  * P3 = xn--9g3bo1gtkw0l8ubf92bgle.kr qna wr_id=113503,
