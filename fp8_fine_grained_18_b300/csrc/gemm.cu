@@ -187,12 +187,15 @@ __device__ __forceinline__ void commit_stage(uint64_t* empty, uint16_t peers) {
 }
 
 // Hand a TMEM partial buffer back to the MMA issuer (the pair's leader).
+// The caller has waited for its TMEM reads (tcgen05.wait::ld) and fenced
+// them (tcgen05.fence::before_thread_sync): the data is in registers and no
+// memory access needs ordering, so the arrival is relaxed.
 template <bool PAIR>
 __device__ __forceinline__ void release_tmem(uint64_t* tempty) {
   if (PAIR)
-    ptx::mbar_arrive_cluster(ptx::mapa(tempty, 0));
+    ptx::mbar_arrive_cluster_relaxed(ptx::mapa(tempty, 0));
   else
-    ptx::mbar_arrive(tempty);
+    ptx::mbar_arrive_relaxed(tempty);
 }
 
 template <int N>
@@ -279,11 +282,12 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   constexpr int STAGES = L::kStages;
   constexpr int TBUF = L::kTBuf;
   // The MMA issuer sleeps in its barrier waits instead of polling on the
-  // one-CTA-per-tile shapes narrower than 256 with 8 promotion warps: there
-  // its polling competed with the promotion warps of its sub-partition, and
-  // sleeping measured +5% (128 x 224) to +16% (128 x 128).  The 256-wide,
-  // CTA-pair and 12-warp shapes measured the same either way and poll.
-  constexpr bool kMmaSuspend = !PAIR && PW == 8 && BN < 256;
+  // CTA-pair shapes and on the one-CTA shapes narrower than 256 with 8
+  // promotion warps: its polling competed with the promotion warps of its
+  // sub-partition, and sleeping measured +5% (128 x 224) to +16% (128 x 128)
+  // and +10-15% on the pairs.  The one-CTA 256-wide and 12-warp shapes
+  // measured the same either way and poll.
+  constexpr bool kMmaSuspend = PAIR || (PW == 8 && BN < 256);
   constexpr int kCols = L::kCols;  // columns per promotion warp
   constexpr uint32_t kTmemCols = 512;
   // a CTA pair runs M = 256 MMAs, each CTA holding 128 rows of A and of D

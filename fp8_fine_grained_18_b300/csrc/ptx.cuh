@@ -41,6 +41,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// The same arrival with relaxed semantics (see mbar_arrive_cluster_relaxed).
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                "r"(bytes)
@@ -159,9 +165,13 @@ __device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (possibly in
-// another CTA of the cluster), with release semantics at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+// another CTA of the cluster) with relaxed semantics: no memory ordering is
+// attached.  For callers whose only hazard is TMEM data already read into
+// registers (tcgen05.wait::ld, then tcgen05.fence::before_thread_sync).
+// The release form orders every earlier memory access at cluster scope on
+// each arrival, and on the CTA-pair GEMM it halved the throughput.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
 
