@@ -866,7 +866,9 @@ TileShape choose_tile(int64_t M, int64_t N, int sms) {
     int bn, cm;
     double eff;
   };
-  const Cand cands[] = {{kTile128x256x2, 256, 2, 1.0}, {kTile128x224x2, 224, 2, 1.0},
+  // 256 x 256 CTA pairs cover the same two-SM footprint as 128 x 256
+  // cluster tiles and measured equal or faster on every workload shape.
+  const Cand cands[] = {{kTile256x256Pair, 256, 2, 1.0}, {kTile128x224x2, 224, 2, 1.0},
                         {kTile128x192x2, 192, 2, 0.9}, {kTile128x160x2, 160, 2, 0.9},
                         {kTile128x128x2, 128, 2, 0.8}, {kTile128x128, 128, 1, 0.7}};
   TileShape best = kTile128x128;
