@@ -98,7 +98,7 @@ fp8bs_status fp8bs_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, int
   if (M == 0 || K == 0) return FP8BS_OK;
   if (!x_bf16 || !q || !scales) return FP8BS_ERR_INVALID_ARG;
   if (K % 128 != 0 || (transpose_out && M % 128 != 0)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (K / 128 > 65535 || (transpose_out && M / 128 > 65535) || M >= kMaxDim * 64)
+  if (K / 128 > 65535 || (transpose_out && M / 128 > 65535) || M >= kMaxDim)
     return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales)) return FP8BS_ERR_MISALIGNED;
   fp8bs_status st = check_device();
@@ -171,7 +171,7 @@ fp8bs_status fp8bs_quant_act_e5m6(const void* x_bf16, int64_t M, int64_t K, uint
   if (M == 0 || K == 0) return FP8BS_OK;
   if (!x_bf16 || !packed || !scales) return FP8BS_ERR_INVALID_ARG;
   if (K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (K / 128 > 65535 || M >= kMaxDim * 64) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (K / 128 > 65535 || M >= kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x_bf16) || !aligned16(packed) || !aligned16(scales) || (q && !aligned16(q)) ||
       (q_scales && !aligned16(q_scales)))
     return FP8BS_ERR_MISALIGNED;

@@ -145,3 +145,33 @@ def test_valid_call_without_gpu_reports_cuda_or_arch(libfp8bs):
     L, m = libfp8bs.lib(), libfp8bs
     st = L.fp8bs_quant_act_1x128(FAKE, 4, 128, 0, FAKE, FAKE, None)
     assert st in (m.ERR_CUDA, m.ERR_ARCH)
+
+
+def test_maximum_sizes_rejected(libfp8bs):
+    """Sizes past what the kernels index (32-bit rows, 65535 grid rows) are
+    refused before anything is launched."""
+    L, m = libfp8bs.lib(), libfp8bs
+    big = 1 << 31
+    assert L.fp8bs_quant_act_1x128(FAKE, big, 128, 0, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_1x128(FAKE, 128 * 65536, 128, 1, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_1x128(FAKE, 128, 128 * 65536, 0, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_weight_128x128(FAKE, 128 * 65536, 128, FAKE, FAKE, None, None, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 128 * 65536, 128, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_dual(FAKE, 128 * 65536, 128, FAKE, FAKE, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_e5m6(FAKE, big, 128, FAKE, FAKE, None, None, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_requant_e5m6_to_128x1(FAKE, FAKE, 128 * 65536, 128, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_and_weight(FAKE, big, 128, FAKE, FAKE, FAKE, 128, 128, FAKE, FAKE,
+                                        None) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_per_tensor(FAKE, 1 << 30, 1 << 16, FAKE, FAKE, None, 0, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    gargs = lambda M, N, K: (FAKE, FAKE, FAKE, FAKE, 0, M, N, K, FAKE, 0, 1, None)  # noqa: E731
+    assert L.fp8bs_gemm_ex(*gargs(big, 256, 128)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_ex(*gargs(8, big, 128)) == m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_gemm_ex(*gargs(8, 256, big)) == m.ERR_UNSUPPORTED_SHAPE
