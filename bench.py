@@ -38,6 +38,9 @@ METRIC = ("block-scaled FP8 GEMM TFLOP/s and % dense FP8 peak; "
           "quantizer GB/s and % HBM peak")
 # Dense FP8 peak = measured bf16 peak x the nominal fp8/bf16 ratio (4.5/2.25).
 FP8_OVER_BF16 = 2.0
+# nominal HBM3e bandwidth of a B300 (the quantizers' spec-sheet denominator;
+# frac_hbm is against the measured copy bandwidth)
+HBM_NOMINAL_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM traffic of one GEMM launch on the dense workload from an ncu capture
@@ -312,7 +315,7 @@ def run_ours(args):
     kernels = {
         "quant_act_and_weight (Q1 of A and Q2 of W, one launch)": {
             "ms": round(statistics.mean(t_q), 4), "GB/s": round(q_gbs, 1),
-            "frac_hbm": round(q_gbs / hbm, 4)},
+            "frac_hbm": round(q_gbs / hbm, 4), "frac_hbm_nominal_8TBs": round(q_gbs / HBM_NOMINAL_GBS, 4)},
         "gemm": {"ms": round(g_ms, 4), "TFLOP/s": round(g_tflops, 1),
                  "frac_fp8_peak": round(g_tflops / fp8_peak, 4)},
     }
@@ -475,7 +478,8 @@ def measure_rows(fp8bs, torch, dev, peaks):
     def quant_row(name, fn, nbytes):
         ms = _time_ms(fn, torch, flush=flush)
         gbs = nbytes / (ms * 1e-3) / 1e9
-        rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+        rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                      "frac_hbm_nominal_8TBs": round(gbs / HBM_NOMINAL_GBS, 4)}
 
     # the dense step's quantizers as separate launches
     dense = synth.make_inputs("dense")
