@@ -279,8 +279,9 @@ struct Q1E5 {
         for (int k = 0; k < 4; ++k) {
           const float2 qn =
               neg_quotient_1step_x2(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), g5.s, g5.nr);
-          c[2 * k] = e5m6_of_neg(qn.x);
-          c[2 * k + 1] = e5m6_of_neg(qn.y);
+          const uint32_t ux = __float_as_uint(qn.x), uy = __float_as_uint(qn.y);
+          c[2 * k] = e5m6_code_fast(ux & 0x7FFFFFFFu, (~ux >> 20) & 0x800u);
+          c[2 * k + 1] = e5m6_code_fast(uy & 0x7FFFFFFFu, (~uy >> 20) & 0x800u);
         }
       } else {
 #pragma unroll
