@@ -221,3 +221,19 @@ def test_stress_full_sampled(fp8bs, oracle_mod):
     a, sa = oracle_mod.quant_act_1x128(inp["A"])
     b, sb = oracle_mod.quant_act_1x128(inp["B"])
     _check_sampled(fp8bs, oracle_mod, a, sa, b, sb, TILE, "stress", samples=1500, bf16=False)
+
+
+def test_bench_step_full_sampled(fp8bs, oracle_mod):
+    """The dense projection step exactly as the benchmark launches it: both
+    operands quantized in one launch, then the GEMM with the automatic tile
+    and BF16 output; sampled outputs against the oracle's chain."""
+    inp = synth.make_inputs("dense")
+    qa, sa, qb, sb = fp8bs.quant_act_and_weight(dev_bf16(inp["A"]), dev_bf16(inp["B"]))
+    c = fp8bs.gemm(qa, sa, qb, sb, BLOCK, out_dtype=torch.bfloat16)
+    a_ref, sa_ref = oracle_mod.quant_act_1x128(inp["A"])
+    b_ref, sb_ref = oracle_mod.quant_weight_128x128(inp["B"])
+    M, N = a_ref.shape[0], b_ref.shape[0]
+    ms, ns = _sample_positions(M, N, 4000, 7)
+    ref = oracle_mod.gemm_sampled(a_ref, sa_ref, b_ref, sb_ref, BLOCK, ms, ns)
+    v = host(c[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()])
+    assert_gemm_bf16(v, ref, "bench step")
