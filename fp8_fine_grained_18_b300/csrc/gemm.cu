@@ -352,6 +352,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   // the peer's barriers must be initialised before any multicast reaches them
   if (CM > 1) ptx::cluster_sync();
   const uint32_t tmem_base = *tmem_base_slot;
+  // Launched as a programmatic dependent: everything above overlapped the
+  // previous kernel's tail; its results are visible from here on.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int KB = p.KB;
   const int unit_first = blockIdx.x / CM;
@@ -827,13 +830,20 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::kAlloc;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CM;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (CM > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = CM;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = CM > 1 ? 1 : 0;
+  cfg.numAttrs = na;
   e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -438,6 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = StreamSmem<Op>;
   constexpr int S = Op::kStages;
   constexpr int kTeamWarps = kConsumerWarps / Op::kTeams;
+  // A programmatic dependent (the GEMM) may start on SMs this grid leaves;
+  // it waits for this grid's completion before reading what it wrote.
+  asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
