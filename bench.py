@@ -47,7 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum),
 # valid only for the kernel source it was taken on (sha of gemm.cu, ptx.cuh,
 # fp8_common.cuh); reported as null once the source has changed.
-TRAFFIC = {"gemm": {"bytes": 86749184 + 35503360, "src_sha": "4b1f450e5db07c3e"}}
+TRAFFIC = {"gemm": {"bytes": 87072000 + 35828224, "src_sha": "401cbb351e5eaa04"}}
 
 
 def kernel_source_sha():

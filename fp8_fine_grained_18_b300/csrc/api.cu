@@ -1,6 +1,7 @@
 // api.cu -- the exported C ABI of libfp8bs (declared in include/fp8bs.h):
 // host-side argument validation, device-architecture check, and dispatch to
 // the kernel launchers.  Nothing is launched when an argument is invalid.
+#include <atomic>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -21,8 +22,8 @@ fp8bs_status cuda_status(cudaError_t e) {
   return FP8BS_ERR_CUDA;
 }
 
-// 0 = unknown, 1 = sm_103, 2 = other
-int g_arch_cache[128];
+// 0 = unknown, 1 = sm_103, 2 = other (several host threads may fill it)
+std::atomic<int> g_arch_cache[128];
 
 fp8bs_status check_device() {
   int dev = -1;
@@ -31,7 +32,7 @@ fp8bs_status check_device() {
     cudaGetLastError();
     return cuda_status(e);
   }
-  int cached = (dev >= 0 && dev < 128) ? g_arch_cache[dev] : 0;
+  int cached = (dev >= 0 && dev < 128) ? g_arch_cache[dev].load() : 0;
   if (cached == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -39,7 +40,7 @@ fp8bs_status check_device() {
       return cuda_status(cudaGetLastError());
     }
     cached = (major == 10 && minor == 3) ? 1 : 2;
-    if (dev >= 0 && dev < 128) g_arch_cache[dev] = cached;
+    if (dev >= 0 && dev < 128) g_arch_cache[dev].store(cached);
   }
   return cached == 1 ? FP8BS_OK : FP8BS_ERR_ARCH;
 }

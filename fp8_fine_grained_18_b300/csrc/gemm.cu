@@ -37,6 +37,9 @@
 // The un-promoted variant (PROMOTE = false) keeps the whole K inside one
 // TMEM accumulator and applies K-group 0's scales once at the end: the
 // measurement of what tensor-core-only accumulation costs (P1 paragraph 4).
+#include <atomic>
+#include <mutex>
+
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -754,8 +757,11 @@ int num_sms_current_device() {
 // shared-memory attribute is set, the register split is checked against
 // what the compiled kernel is launched with, and for clusters the number of
 // clusters that fit on the device at once.
+// Host threads may launch concurrently: the first to arrive computes the
+// facts under the mutex and publishes them with a release store.
 struct KernelInfo {
-  bool ready = false;
+  std::atomic<bool> ready{false};
+  std::mutex mu;
   cudaError_t err = cudaSuccess;
   int max_ctas = 0;  // persistent grid size (a multiple of CM)
 };
@@ -771,37 +777,40 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   KernelInfo& ki = info[dev];
-  if (!ki.ready) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e == cudaSuccess && L::kRegSplit) {
-      cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, kern);
-      // setmaxnreg.inc waits until the registers it asks for are free: a
-      // split larger than the launch's allocation would never proceed.
-      if (e == cudaSuccess && fa.numRegs * kThreads < L::kSplitRegsNeeded)
-        e = cudaErrorInvalidConfiguration;
+  if (!ki.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(ki.mu);
+    if (!ki.ready.load(std::memory_order_relaxed)) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+      if (e == cudaSuccess && L::kRegSplit) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        // setmaxnreg.inc waits until the registers it asks for are free: a
+        // split larger than the launch's allocation would never proceed.
+        if (e == cudaSuccess && fa.numRegs * kThreads < L::kSplitRegsNeeded)
+          e = cudaErrorInvalidConfiguration;
+      }
+      int ctas = num_sms_current_device();
+      if (e == cudaSuccess && CM > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CM * 64);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::kAlloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CM;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (e == cudaSuccess && clusters < 1) e = cudaErrorInvalidConfiguration;
+        ctas = clusters * CM;
+      }
+      ki.err = e;
+      ki.max_ctas = ctas;
+      ki.ready.store(true, std::memory_order_release);
     }
-    int ctas = num_sms_current_device();
-    if (e == cudaSuccess && CM > 1) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(CM * 64);
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = L::kAlloc;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = CM;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int clusters = 0;
-      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
-      if (e == cudaSuccess && clusters < 1) e = cudaErrorInvalidConfiguration;
-      ctas = clusters * CM;
-    }
-    ki.err = e;
-    ki.max_ctas = ctas;
-    ki.ready = true;
   }
   if (ki.err != cudaSuccess) return ki.err;
 
