@@ -829,13 +829,26 @@ __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
       dequant4(tw[r * 32 + cq], srow[r], xv);
   };
   float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const int r = part * 16 + i;
-    float xv[4];
-    dq(r, xv);
+  // The E5M6 decode is costly enough that the 16 x 4 values are decoded once
+  // and kept in registers for the code pass (96 registers, 2 CTAs per SM);
+  // for E4M3 the hardware conversions are cheap and occupancy wins (61
+  // registers, 4 CTAs per SM, decoding twice).
+  float xr[E5 ? 16 : 1][4];
+  if constexpr (E5) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xv[c]);
+    for (int i = 0; i < 16; ++i) {
+      dq(part * 16 + i, xr[i]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xr[i][c]);
+    }
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      float xv[4];
+      dq(part * 16 + i, xv);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xv[c]);
+    }
   }
   *reinterpret_cast<float4*>(&red[part][4 * cq]) = make_float4(m[0], m[1], m[2], m[3]);
   __syncthreads();
@@ -859,14 +872,20 @@ __global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
   uint32_t o[4][4];
 #pragma unroll
   for (int i = 0; i < 16; i += 4) {
-    const int r = part * 16 + i;
-    float x0[4], x1[4], x2[4], x3[4];
-    dq(r, x0);
-    dq(r + 1, x1);
-    dq(r + 2, x2);
-    dq(r + 3, x3);
+    if constexpr (E5) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
+      for (int c = 0; c < 4; ++c)
+        o[c][i >> 2] = codes_f32x4(xr[i][c], xr[i + 1][c], xr[i + 2][c], xr[i + 3][c], g[c]);
+    } else {
+      const int r = part * 16 + i;
+      float x0[4], x1[4], x2[4], x3[4];
+      dq(r, x0);
+      dq(r + 1, x1);
+      dq(r + 2, x2);
+      dq(r + 3, x3);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
+    }
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c)
