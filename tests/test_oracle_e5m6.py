@@ -5,6 +5,9 @@ The E5M6 value set is pinned against numpy's IEEE half precision (the same
 exponent field; E5M6 keeps the top 6 of half's 10 mantissa bits), rounding
 against a float64 closed form, the bit packing against hand-worked bytes,
 and the quantizers against definitions already pinned elsewhere."""
+import os
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -163,3 +166,20 @@ def test_requant_e5m6_general_scales_half_ulp(oracle_mod):
     half = 0.5 * np.where(y < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
     assert np.all(np.abs(xh - d) <= (half + 2.0 ** -24 * y) * sT[0][None, :])
     assert np.all(np.abs(oracle_mod.e4m3_decode_array(qT)).max(axis=1) == 448.0)
+
+
+def test_hand_worked_golden_values(oracle_mod):
+    """Codes worked out by hand from the format definition
+    (tests/golden/e5m6_hand_values.txt)."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "e5m6_hand_values.txt")
+    n = 0
+    for line in open(path):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        value, code = line.split()
+        v = np.float32(float(Fraction(value)) if value != "-0.0" else -0.0)
+        assert float(v) == float(Fraction(value)), value  # the value is exact in FP32
+        assert oracle_mod.e5m6_encode(float(v)) == int(code, 16), (value, code)
+        n += 1
+    assert n == 14
