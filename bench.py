@@ -4,8 +4,10 @@
 One step = one pass of the path over one batch of the dense workload
 (attention-projection shape: M = 4096 tokens, N = K = 7168; activations
 N(0,1) with 0.1% outlier channels x100, weights N(0,0.02); bf16 in, bf16
-out): quantize the activations in 1x128 tiles, quantize the weights in
-128x128 blocks, then the block-scaled FP8 GEMM with FP32 promotion.
+out): quantize the activations in 1x128 tiles and the weights in 128x128
+blocks (one launch), then the block-scaled FP8 GEMM with FP32 promotion.
+With `--rows 1` (the default) every other hot-path operation is also timed
+at its own workload shape and reported under `rows`.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
