@@ -160,6 +160,10 @@ fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t *q,
  *   Requires K % 128 == 0, N % 16 == 0, K > 0; M >= 0 (a ragged M tail is
  *   handled); M == 0 or N == 0 is a no-op.
  * Returns FP8BS_ERR_TIMEOUT only through fp8bs_get_device_error().
+ * Every GEMM call is a programmatic dependent launch.  Its set-up (barriers,
+ * tensor memory, tensor-map prefetch) may overlap the tail of the previous
+ * kernel on `stream`, but it reads its inputs only after that kernel has
+ * completed.  Stream order is unchanged for the caller.
  */
 fp8bs_status fp8bs_gemm(const uint8_t *a, const float *sa, const uint8_t *b,
                         const float *sb, fp8bs_bscale_kind bkind, int64_t M,
