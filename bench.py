@@ -236,10 +236,10 @@ def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    if world > 1:  # after set_device, so each rank's NCCL communicator uses its own GPU
+        dist.init_process_group("nccl", device_id=dev)
     peaks, peak_kind = load_peaks()
 
     w = synth.WORKLOADS[WORKLOAD]
@@ -345,7 +345,9 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(), "wall_timed_s": round(wall, 4),
     }
-    if args.rows and rank == 0:
+    # the per-row details are a single-GPU measurement: under torchrun they
+    # would hold every GPU while rank 0 alone runs them
+    if args.rows and world == 1:
         out["rows"] = measure_rows(fp8bs, torch, dev, peaks)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(M, N, K, inp, budget_s=20.0)
