@@ -9,7 +9,9 @@
 //
 // B300 design (the pages' H800 WGMMA kernel is prior art only):
 //   * persistent CTAs, one per SM, each computing 128 x BN output tiles
-//     (BN = 128, 224 or 256, chosen per shape to limit wave quantization);
+//     (BN = 128 ... 256, chosen per shape to limit wave quantization), or,
+//     as a CTA pair (tcgen05 cta_group::2), 256 x BN tiles whose MMAs span
+//     both SMs;
 //   * with CM = 2, the two CTAs of a cluster work on vertically adjacent
 //     tiles that share the same B tile: each loads half of it and multicasts
 //     that half into both CTAs' shared memory, which halves the L2->SM
@@ -30,6 +32,12 @@
 //     computes the next group's partial into the other TMEM buffer (the
 //     "overlapping of the two operations" of P3 paragraph 4 / P4 paragraph 1);
 //     the epilogue converts to BF16 (RNE) or keeps FP32 and stores.
+//   * the per-K-group hand-off is the cost centre: the MMA issuer sleeps
+//     in its barrier waits (a polling thread takes issue slots and shared
+//     memory bandwidth from the promotion warps beside it), and TMEM buffers
+//     are released with relaxed arrivals (the data is already in registers);
+//   * launched as a programmatic dependent: barriers, TMEM and tensor maps
+//     are set up while the previous kernel on the stream finishes;
 //   * every mbarrier wait is bounded (globaltimer); on expiry the kernel
 //     sets a device error word and an abort flag, every role winds down,
 //     in-flight copies and MMAs are drained (bounded) and TMEM is freed.
