@@ -54,7 +54,7 @@ TRAFFIC = {"gemm": {"bytes": 87072000 + 35828224, "src_sha": "e666d1eb943cfd55"}
 
 def kernel_source_sha():
     """Fingerprint of the GEMM's code (comments and blank lines removed, so
-    that editing a comment keeps the traffic figure below valid)."""
+    that editing a comment keeps TRAFFIC valid)."""
     import re
     h = hashlib.sha256()
     for f in ("gemm.cu", "ptx.cuh", "fp8_common.cuh"):
