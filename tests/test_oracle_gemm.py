@@ -133,3 +133,39 @@ def test_limited_acc_special_cases(oracle_mod):
     lim = oracle_mod.gemm_limited_acc(a2, sa2, b2, sb2, BLOCK, ms2, ns2, bits=14, group=32,
                                       promote_every=0)
     assert not np.array_equal(lim, ex2)
+
+
+def _one_row(codes_a, codes_b):
+    """A 1x128 times 128x128-block operand pair with unit scales."""
+    a = np.array([codes_a], np.uint8)
+    b = np.zeros((128, 128), np.uint8)
+    b[0] = codes_b
+    return a, np.ones((1, 1), np.float32), b, np.ones((1, 1), np.float32)
+
+
+def test_limited_acc_hand_worked(oracle_mod):
+    """The accumulator model against its own stated steps, worked by hand:
+    per group of 32 products, align everything to the largest exponent E,
+    keep 14 bits below it (units of 2^(E-13)) by flooring each term
+    (sign-fill right shift), add exactly, truncate to FP32."""
+    one, tiny, neg_tiny = 0x38, 0x01, 0x81  # 1.0, 2^-9, -2^-9
+    # 1.0 * 1.0 then 31 products of 2^-9 * 2^-9 = 2^-18: with E = 0 the unit
+    # is 2^-13 and floor(2^-18 / 2^-13) = 0, so every tiny term is lost.
+    codes_a = np.array([one] + [tiny] * 31 + [0] * 96, np.uint8)
+    codes_b = np.array([one] + [tiny] * 31 + [0] * 96, np.uint8)
+    a, sa, b, sb = _one_row(codes_a, codes_b)
+    got = oracle_mod.gemm_limited_acc(a, sa, b, sb, BLOCK, [0], [0], bits=14, group=32)
+    assert got[0] == 1.0
+    assert oracle_mod.gemm(a, sa, b, sb, BLOCK)[0, 0] == 1.0 + 31 * 2.0 ** -18
+    # negative tiny products: floor(-2^-5) = -1 unit each, so the group sums
+    # to (2^13 - 31) units = 1 - 31 * 2^-13
+    codes_b2 = np.array([one] + [neg_tiny] * 31 + [0] * 96, np.uint8)
+    a, sa, b, sb = _one_row(codes_a, codes_b2)
+    got = oracle_mod.gemm_limited_acc(a, sa, b, sb, BLOCK, [0], [0], bits=14, group=32)
+    assert got[0] == 1.0 - 31 * 2.0 ** -13
+    # the same tiny terms in a group of their own, with nothing larger: E is
+    # their own exponent (-18), so they are kept exactly (31 * 2^-18)
+    codes_a3 = np.array([tiny] * 31 + [0] * 97, np.uint8)
+    a, sa, b, sb = _one_row(codes_a3, codes_a3)
+    got = oracle_mod.gemm_limited_acc(a, sa, b, sb, BLOCK, [0], [0], bits=14, group=32)
+    assert got[0] == 31 * 2.0 ** -18
