@@ -175,3 +175,9 @@ def test_maximum_sizes_rejected(libfp8bs):
     assert L.fp8bs_gemm_ex(*gargs(big, 256, 128)) == m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_gemm_ex(*gargs(8, big, 128)) == m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_gemm_ex(*gargs(8, 256, big)) == m.ERR_UNSUPPORTED_SHAPE
+
+
+def test_python_binding_covers_every_declared_function(libfp8bs):
+    """Every call the header declares has a typed ctypes binding."""
+    missing = [n for n in _declared_functions() if n not in libfp8bs._SIGS]
+    assert not missing, missing
