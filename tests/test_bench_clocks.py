@@ -62,3 +62,18 @@ def test_sampler_reports_reasons_inside_region_only(fake_smi):
     out = s.summary()
     assert "sw_power_cap" in out["reasons"]
     assert out["sm_mhz"] == 1500.0
+
+
+def test_algorithmic_bytes_per_element():
+    """The bench's byte counts are the per-element figures the roofline
+    uses: Q1 2 + 1 + 4/128, Q2 3 + 4/16384 (4 + 8/16384 with the transposed
+    copy), the dual quantizer 2 + 2 * (1 + 4/128), Q3 2 * (1 + 4/128)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    M, K = 4096, 7168
+    n = M * K
+    assert bench.algorithmic_bytes_q1(M, K) / n == pytest.approx(3 + 4 / 128)
+    assert bench.algorithmic_bytes_q2(M, K) / n == pytest.approx(3 + 4 / 16384)
+    assert bench.algorithmic_bytes_q2(M, K, transposed=True) / n == pytest.approx(4 + 8 / 16384)
+    assert bench.algorithmic_bytes_dual(M, K) / n == pytest.approx(2 + 2 * (1 + 4 / 128))
+    assert bench.algorithmic_bytes_q3(M, K) / n == pytest.approx(2 * (1 + 4 / 128))
