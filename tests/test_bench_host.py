@@ -1,4 +1,5 @@
-"""The bench's clock sampler, on the CPU against a fake nvidia-smi: it must be
+"""Host-side logic of the bench.  The clock sampler, on the CPU against a fake
+nvidia-smi: it must be
 sampling before the timed region starts, keep only the samples taken while
 the region ran, and report the throttle reasons it saw."""
 import os
