@@ -1,7 +1,7 @@
-"""Host-side logic of the bench.  The clock sampler, on the CPU against a fake
-nvidia-smi: it must be
-sampling before the timed region starts, keep only the samples taken while
-the region ran, and report the throttle reasons it saw."""
+"""Host-side logic of the bench.  The clock sampler, run on the CPU against a
+fake nvidia-smi, must be sampling before the timed region starts, keep only
+the samples taken while the region ran, and report the throttle reasons it
+saw.  The algorithmic byte counts match the per-element figures."""
 import os
 import stat
 import sys
