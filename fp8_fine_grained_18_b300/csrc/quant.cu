@@ -3,6 +3,12 @@
 //   Q1T the same tiles laid 128x1, written transposed  (page P1, para 3)
 //   Q2  128x128 weight blocks (+ transposed copy)      (page P1, para 3)
 //   Q3  1x128 -> 128x1 re-tiling of cached FP8 codes   (page P1, para 3)
+//   Q12 Q1 of an activation and Q2 of a weight in one launch
+//   dual: Q1 and Q1T of one tensor from one read        (page P2, para 1)
+//   Q1E5 / E5M6 re-tiling: the E5M6 cache of the re-tiled activations
+//                                                       (page P1, para 3)
+//   per-tensor baseline: one scale for the whole tensor (page P1, para 4;
+//                                                        page P3, para 4)
 //
 // Q1 and Q2 are one streaming scheme: a persistent CTA per SM whose producer
 // warp moves input tiles into a ring of shared-memory stages with 2-D TMA
@@ -11,8 +17,9 @@
 // threads must exchange group maxima, the consumers form two teams of 8
 // warps that work on alternate tiles, so one team's barrier waits overlap
 // the other's work.  Tiles are ordered with the K-group fastest, so the CTAs
-// running at one time read one contiguous band of the input.  Q1T and Q3,
-// which transpose, are plain one-tile-per-CTA kernels (see below).  Each
+// running at one time read one contiguous band of the input.  Q12 and Q1E5
+// are further ops of the same scheme.  Q1T, the dual quantizer and Q3, which
+// transpose, are plain one-tile-per-CTA kernels (see below).  Each
 // input byte is read from HBM once and each output byte written once.
 //
 // Group max-abs is an integer max on the sign-stripped bit patterns
