@@ -20,12 +20,10 @@ LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
 OUT_BF16, OUT_F32, OUT_E4M3_1x128 = 0, 1, 2
-TILE_AUTO, TILE_128x128, TILE_128x224_CLUSTER2, TILE_128x256_CLUSTER2 = -1, 0, 1, 2
-TILE_128x128_CLUSTER2, TILE_128x160_CLUSTER2, TILE_128x192_CLUSTER2 = 3, 4, 5
-TILE_256x256_PAIR, TILE_256x224_PAIR, TILE_256x192_PAIR = 6, 7, 8
-TILE_128x192_CLUSTER2_W12, TILE_256x192_PAIR_W12 = 9, 10
-TILE_256x128_PAIR, TILE_256x160_PAIR = 11, 12
-TILES = tuple(range(13))
+TILE_AUTO, TILE_128x128, TILE_128x256 = -1, 0, 1
+TILE_256x128_PAIR, TILE_256x160_PAIR, TILE_256x192_PAIR = 2, 3, 4
+TILE_256x224_PAIR, TILE_256x256_PAIR, TILE_256x192_PAIR_W12 = 5, 6, 7
+TILES = tuple(range(8))
 BSCALE_BLOCK_128x128, BSCALE_TILE_1x128 = 0, 1
 GROUP = 128
 

@@ -60,7 +60,7 @@ fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, co
     return FP8BS_ERR_INVALID_ARG;
   if (out == FP8BS_OUT_E4M3_1x128 && (promote != 1 || !c_scales)) return FP8BS_ERR_INVALID_ARG;
   if (promote != 0 && promote != 1) return FP8BS_ERR_INVALID_ARG;
-  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_256x160_PAIR) return FP8BS_ERR_INVALID_ARG;
+  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_256x192_PAIR_W12) return FP8BS_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FP8BS_OK;
   if (!a || !sa || !b || !sb || !c) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;

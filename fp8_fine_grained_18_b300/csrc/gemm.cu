@@ -10,15 +10,16 @@
 // B300 design (the pages' H800 WGMMA kernel is prior art only):
 //   * persistent CTAs, one per SM, each computing 128 x BN output tiles
 //     (BN = 128 ... 256, chosen per shape to limit wave quantization), or,
-//     as a CTA pair (tcgen05 cta_group::2), 256 x BN tiles whose MMAs span
-//     both SMs;
-//   * with CM = 2, the two CTAs of a cluster work on vertically adjacent
-//     tiles that share the same B tile: each loads half of it and multicasts
-//     that half into both CTAs' shared memory, which halves the L2->SM
-//     traffic of B;
+//     as a CTA pair (tcgen05 cta_group::2, a cluster of two), 256 x BN tiles
+//     whose MMAs span both SMs: each CTA loads its own 128 rows of A and its
+//     own half of the B tile, and the tensor cores read the peer's half
+//     directly, which halves the shared-memory traffic of B per MAC;
+//   * no TMA load is multicast: every copy lands only in the shared memory
+//     of the CTA that issues it;
 //   * warp 0 -- TMA producer: A and B K-group tiles (128 B rows, 128-byte
 //     swizzle) into a STAGES-deep shared-memory ring (mbarrier full/empty;
-//     with CM = 2 a stage is free only once both CTAs' MMAs have read it);
+//     for a pair, both CTAs' copies complete on the leader's full barrier
+//     and the leader's MMA commit frees the stage in both CTAs);
 //   * warp 1 -- MMA issuer: per K-group, four tcgen05.mma kind::f8f6f4
 //     (K = 32 each) into one of the TMEM partial buffers, then
 //     tcgen05.commit to free the smem stage and to publish the partial;
@@ -82,7 +83,7 @@ struct Params {
   void* c;
   float* c_scales;  // E4M3 output: [N/128][M]
   int M, N, K, KB;
-  int num_m_units, num_units;  // a unit = CM vertically adjacent 128 x BN tiles
+  int num_m_units, num_units;  // a unit = one 128 x BN tile, or a pair's 256 x BN tile
   int skip_iter;
 };
 
@@ -119,8 +120,9 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 
 // PW promotion warps (8 or 12) share the tile's columns: each owns 32 TMEM
 // lanes (rows) and kCols = BN / (PW / 4) columns.
-template <int BN, int CM, bool PAIR, int PW>
+template <int BN, bool PAIR, int PW>
 struct Cfg {
+  static constexpr int CM = PAIR ? 2 : 1;  // CTAs per cluster
   static_assert(PW == 8 || PW == 12, "promotion warps");
   static constexpr int kPromoWarps = PW;
   static constexpr int kThreads = 32 * (kFirstPromoWarp + PW);
@@ -139,17 +141,15 @@ struct Cfg {
   static constexpr int kSplitRegsNeeded = 128 * kCtlRegs + 32 * PW * kPromoRegs;
   static_assert(!kRegSplit || kSplitRegsNeeded <= 65536, "register split");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(CM == 1 || CM == 2, "CM");
-  static_assert(!PAIR || CM == 2, "a CTA pair is a cluster of two");
-  // B rows this CTA loads: multicast to both CTAs when CM = 2, or, for a CTA
-  // pair, its own half of the pair's B tile
+  // B rows this CTA loads: the whole B tile, or, for a CTA pair, its own
+  // half of the pair's B tile
   static constexpr int kBH = BN / CM;
   static_assert(kBH % 8 == 0, "B half must be whole 8-row swizzle atoms");
   // columns between TMEM partial buffers, and how many fit in 512 columns
   static constexpr int kTmemStride = BN <= 128 ? 128 : BN <= 160 ? 160 : 256;
   static constexpr int kTBuf = 512 / kTmemStride > 4 ? 4 : 512 / kTmemStride;
   static constexpr int kABytes = kBM * kBK;
-  static constexpr int kBBytes = (PAIR ? kBH : BN) * kBK;
+  static constexpr int kBBytes = kBH * kBK;
   static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
   static constexpr int kScaleFloats = kBM + kScaleB;
   static constexpr int kNumBarsMax = 2 * 8 + 2 * 4 + 2 * kScaleSlots + 1;
@@ -186,15 +186,14 @@ __device__ __forceinline__ void issue_kgroup(uint32_t d, uint32_t a0, uint32_t b
 }
 
 // Free a shared-memory stage once the MMAs reading it completed: in this
-// CTA, in both CTAs of a multicast cluster, or in both CTAs of a pair.
-template <int CM, bool PAIR>
-__device__ __forceinline__ void commit_stage(uint64_t* empty, uint16_t peers) {
+// CTA, or in both CTAs of a pair (the commit arrives on the barrier at the
+// same offset in each CTA).
+template <bool PAIR>
+__device__ __forceinline__ void commit_stage(uint64_t* empty) {
   if (PAIR)
-    ptx::tc_commit_pair_mcast(empty, peers);
-  else if (CM == 1)
-    ptx::tc_commit(empty);
+    ptx::tc_commit_pair_mcast(empty, 0x3);
   else
-    ptx::tc_commit_mcast(empty, peers);
+    ptx::tc_commit(empty);
 }
 
 // Hand a TMEM partial buffer back to the MMA issuer (the pair's leader).
@@ -284,11 +283,12 @@ __device__ __forceinline__ void tmem_ld_step(uint32_t taddr, uint32_t* r) {
 // quantized in the epilogue).
 enum : int { kOutF32 = 0, kOutBf16 = 1, kOutE4m3 = 2 };
 
-template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
+template <int BN, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
 __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b, const Params p) {
-  using L = Cfg<BN, CM, PAIR, PW>;
+  using L = Cfg<BN, PAIR, PW>;
+  constexpr int CM = L::CM;
   constexpr int kPromoWarps = L::kPromoWarps;
   constexpr int STAGES = L::kStages;
   constexpr int TBUF = L::kTBuf;
@@ -306,7 +306,6 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   // bytes one stage's full barrier waits for: what lands in this CTA, or,
   // for a pair (whose leader's barrier counts both CTAs' copies), twice that
   constexpr uint32_t kStageTx = (PAIR ? 2 : 1) * (L::kABytes + L::kBBytes);
-  constexpr uint16_t kPeers = (1u << CM) - 1u;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -332,8 +331,8 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       ptx::mbar_init(&full[i], 1);
-      // one MMA commit from each CTA of the cluster (a pair has one issuer)
-      ptx::mbar_init(&empty[i], PAIR ? 1 : CM);
+      // one MMA commit (a pair's leader commits to both CTAs)
+      ptx::mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < TBUF; ++i) {
       ptx::mbar_init(&tfull[i], 1);
@@ -360,8 +359,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  // the peer's barriers must be initialised before any multicast reaches them
-  if (CM > 1) ptx::cluster_sync();
+  // a pair's barriers must be initialised before the peer's copies and
+  // commits reach them
+  if (PAIR) ptx::cluster_sync();
   const uint32_t tmem_base = *tmem_base_slot;
   // Launched as a programmatic dependent: everything above overlapped the
   // previous kernel's tail; its results are visible from here on.
@@ -402,11 +402,7 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
           }
           ptx::mbar_arrive_expect_tx(&full[stage], kStageTx);
           ptx::tma_load_2d(sA + stage * L::kABytes, &tmap_a, &full[stage], kb * kBK, mt * kBM);
-          if (CM == 1)
-            ptx::tma_load_2d(sB + stage * L::kBBytes, &tmap_b, &full[stage], kb * kBK, nt * BN);
-          else
-            ptx::tma_load_2d_mcast(sB + stage * L::kBBytes + rank * L::kBH * kBK, &tmap_b,
-                                   &full[stage], kb * kBK, nt * BN + rank * L::kBH, kPeers);
+          ptx::tma_load_2d(sB + stage * L::kBBytes, &tmap_b, &full[stage], kb * kBK, nt * BN);
           issued_mask |= 1u << stage;
         }
       }
@@ -452,9 +448,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
             const uint32_t d = tmem_base + buf * L::kTmemStride;
             issue_kgroup<PAIR>(d, a0, b0, kIdesc, false);
-            commit_stage<CM, PAIR>(&empty[stage], kPeers);
+            commit_stage<PAIR>(&empty[stage]);
             if (PAIR)
-              ptx::tc_commit_pair_mcast(&tfull[buf], kPeers);
+              ptx::tc_commit_pair_mcast(&tfull[buf], 0x3);
             else
               ptx::tc_commit(&tfull[buf]);
           }
@@ -470,11 +466,11 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
             issue_kgroup<PAIR>(d, a0, b0, kIdesc, kb > 0);
-            commit_stage<CM, PAIR>(&empty[stage], kPeers);
+            commit_stage<PAIR>(&empty[stage]);
           }
           if (!ok) break;
           if (PAIR)
-            ptx::tc_commit_pair_mcast(&tfull[buf], kPeers);
+            ptx::tc_commit_pair_mcast(&tfull[buf], 0x3);
           else
             ptx::tc_commit(&tfull[buf]);
           ++kt;
@@ -723,16 +719,13 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   // ---- teardown: all roles done (or aborted); free TMEM
   ptx::tc_fence_before();
   __syncthreads();
-  if (CM > 1) {
-    // After an abort a peer's copy may still be landing in this CTA's
-    // shared memory: give it time before leaving (normal runs skip this).
-    if (*abort_flag) {
-      const uint64_t t0 = ptx::globaltimer();
-      while (ptx::globaltimer() - t0 < 1000000ull) {
-      }
-    }
-    // neither CTA leaves (or frees TMEM the pair's MMAs write) while the
-    // other may still write into it
+  if (PAIR) {
+    // Neither CTA leaves (or frees TMEM the pair's MMAs write) while the
+    // other may still touch it.  Copies land only in the issuing CTA's own
+    // shared memory; the follower's copies complete on the leader's full
+    // barriers, which the leader's producer has drained above, and the
+    // leader's MMAs (which read both CTAs' shared memory) were drained by
+    // its MMA issuer, before either CTA arrives here.
     ptx::cluster_sync();
   }
   if (warp == 1) {
@@ -774,11 +767,12 @@ struct KernelInfo {
   int max_ctas = 0;  // persistent grid size (a multiple of CM)
 };
 
-template <int BN, int CM, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
+template <int BN, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
 cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
-  using L = Cfg<BN, CM, PAIR, PW>;
+  using L = Cfg<BN, PAIR, PW>;
+  constexpr int CM = L::CM;
   constexpr int kThreads = L::kThreads;
-  auto kern = gemm_kernel<BN, CM, PAIR, PW, PROMOTE, OUT, B_TILE>;
+  auto kern = gemm_kernel<BN, PAIR, PW, PROMOTE, OUT, B_TILE>;
   static KernelInfo info[kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -868,42 +862,34 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
 
 // Tile shape per problem.  Each candidate's cost is the number of waves it
 // needs times its tile width over a relative efficiency (measured per shape
-// on B300: wider tiles and clusters that share B tiles move fewer bytes per
-// flop; more TMEM partial buffers tolerate more promotion latency); the
+// on B300: the 256-row CTA pairs read half the B operand per MAC from shared
+// memory that one-CTA tiles do, and wider tiles read less A per MAC); the
 // cheapest wins.
 enum TileShape {
   kTile128x128 = 0,
-  kTile128x224x2 = 1,
-  kTile128x256x2 = 2,
-  kTile128x128x2 = 3,
-  kTile128x160x2 = 4,
-  kTile128x192x2 = 5,
+  kTile128x256 = 1,
+  kTile256x128Pair = 2,
+  kTile256x160Pair = 3,
+  kTile256x192Pair = 4,
+  kTile256x224Pair = 5,
   kTile256x256Pair = 6,
-  kTile256x224Pair = 7,
-  kTile256x192Pair = 8,
-  kTile128x192x2W12 = 9,
-  kTile256x192PairW12 = 10,
-  kTile256x128Pair = 11,
-  kTile256x160Pair = 12,
+  kTile256x192PairW12 = 7,
 };
 
 TileShape choose_tile(int64_t M, int64_t N, int sms) {
   struct Cand {
     TileShape s;
-    int bn, cm;
+    int bm, bn;
     double eff;
   };
-  // 256 x 256 CTA pairs cover the same two-SM footprint as 128 x 256
-  // cluster tiles and measured equal or faster on every workload shape.
-  const Cand cands[] = {{kTile256x256Pair, 256, 2, 1.0}, {kTile128x224x2, 224, 2, 1.0},
-                        {kTile128x192x2, 192, 2, 0.9}, {kTile128x160x2, 160, 2, 0.9},
-                        {kTile128x128x2, 128, 2, 0.8}, {kTile128x128, 128, 1, 0.7}};
+  const Cand cands[] = {{kTile256x256Pair, 256, 256, 1.0}, {kTile256x224Pair, 256, 224, 0.98},
+                        {kTile256x192Pair, 256, 192, 0.9}, {kTile256x160Pair, 256, 160, 0.85},
+                        {kTile256x128Pair, 256, 128, 0.8}, {kTile128x128, 128, 128, 0.6}};
   TileShape best = kTile128x128;
   double best_cost = 1e300;
-  const int64_t m_tiles = (M + kBM - 1) / kBM;
   for (const Cand& c : cands) {
-    const int64_t units = ((m_tiles + c.cm - 1) / c.cm) * ((N + c.bn - 1) / c.bn);
-    const int64_t slots = sms / c.cm;
+    const int64_t units = ((M + c.bm - 1) / c.bm) * ((N + c.bn - 1) / c.bn);
+    const int64_t slots = sms / (c.bm / kBM);
     const int64_t waves = (units + slots - 1) / slots;
     const double cost = (double)waves * c.bn / c.eff;
     if (cost < best_cost) {
@@ -916,41 +902,32 @@ TileShape choose_tile(int64_t M, int64_t N, int sms) {
 
 template <bool PROMOTE, int OUT, bool B_TILE>
 cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
-  // E4M3 output needs each promotion thread to own one whole 1x128 group:
-  // 128 x 256 tiles (two 128-column halves per row)
+  // E4M3 output needs each promotion thread to own one whole 1x128 group of
+  // an output row: the 256 x 256 pair (two 128-column halves per row)
   if constexpr (OUT == kOutE4m3) {
-    return launch_variant<256, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
+    return launch_variant<256, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
   } else {
-  int shape = g.tile;
-  if (shape < 0) shape = choose_tile(g.M, g.N, num_sms_current_device());
-  switch (shape) {
-    case kTile128x192x2W12:
-      return launch_variant<192, 2, false, 12, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile256x192PairW12:
-      return launch_variant<192, 2, true, 12, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile256x128Pair:
-      return launch_variant<128, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile256x160Pair:
-      return launch_variant<160, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile256x256Pair:
-      return launch_variant<256, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile256x224Pair:
-      return launch_variant<224, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile256x192Pair:
-      return launch_variant<192, 2, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile128x256x2:
-      return launch_variant<256, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile128x224x2:
-      return launch_variant<224, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile128x192x2:
-      return launch_variant<192, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile128x160x2:
-      return launch_variant<160, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    case kTile128x128x2:
-      return launch_variant<128, 2, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
-    default:
-      return launch_variant<128, 1, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
-  }  }
+    int shape = g.tile;
+    if (shape < 0) shape = choose_tile(g.M, g.N, num_sms_current_device());
+    switch (shape) {
+      case kTile256x192PairW12:
+        return launch_variant<192, true, 12, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x128Pair:
+        return launch_variant<128, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x160Pair:
+        return launch_variant<160, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x192Pair:
+        return launch_variant<192, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x224Pair:
+        return launch_variant<224, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x256Pair:
+        return launch_variant<256, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile128x256:
+        return launch_variant<256, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
+      default:
+        return launch_variant<128, false, 8, PROMOTE, OUT, B_TILE>(g, stream);
+    }
+  }
 }
 
 template <bool PROMOTE, int OUT>

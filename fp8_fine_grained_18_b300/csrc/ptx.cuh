@@ -97,17 +97,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_
       : "memory");
 }
 
-// Same copy, delivered to the same shared-memory offset (data and mbarrier
-// complete_tx) in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_mcast(void* dst, const void* tmap, uint64_t* bar,
-                                                  int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-      "l"(tmap), "r"(smem_addr(bar)), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // CTA-pair form: the data lands in this CTA's shared memory, the complete_tx
 // goes to `bar_cluster`, an mbarrier in either CTA of the pair (a
 // shared::cluster address).
@@ -343,16 +332,6 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) 
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-}
-
-// Arrive once on the mbarrier at this offset in every CTA of cta_mask when
-// every earlier tcgen05 op of this thread has completed.
-__device__ __forceinline__ void tc_commit_mcast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(cta_mask)
-      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {

@@ -190,30 +190,24 @@ fp8bs_status fp8bs_gemm_ex(const uint8_t *a, const float *sa,
  * they differ in speed.  FP8BS_TILE_AUTO (what fp8bs_gemm uses) picks, per
  * problem, the shape that needs the fewest full waves of tiles over the
  * device's SMs, weighted by each shape's efficiency.
- *   128x128            one CTA per tile;
- *   128xBN_CLUSTER2    clusters of two CTAs on vertically adjacent tiles
- *                      that share (and multicast) the B tile;
- *   256xBN_PAIR        a CTA pair whose tensor cores compute one 256xBN
- *                      tile together, each CTA holding half of A and half
- *                      of B;
+ *   128xBN             one CTA per tile;
+ *   256xBN_PAIR        a CTA pair (a cluster of two CTAs) whose tensor cores
+ *                      compute one 256xBN tile together, each CTA loading
+ *                      its own half of A and half of B (no copy is
+ *                      multicast);
  *   ..._W12            the same with 12 promotion warps of 64 columns each
  *                      (8 otherwise).
  */
 typedef enum {
   FP8BS_TILE_AUTO = -1,
   FP8BS_TILE_128x128 = 0,
-  FP8BS_TILE_128x224_CLUSTER2 = 1,
-  FP8BS_TILE_128x256_CLUSTER2 = 2,
-  FP8BS_TILE_128x128_CLUSTER2 = 3,
-  FP8BS_TILE_128x160_CLUSTER2 = 4,
-  FP8BS_TILE_128x192_CLUSTER2 = 5,
+  FP8BS_TILE_128x256 = 1,
+  FP8BS_TILE_256x128_PAIR = 2,
+  FP8BS_TILE_256x160_PAIR = 3,
+  FP8BS_TILE_256x192_PAIR = 4,
+  FP8BS_TILE_256x224_PAIR = 5,
   FP8BS_TILE_256x256_PAIR = 6,
-  FP8BS_TILE_256x224_PAIR = 7,
-  FP8BS_TILE_256x192_PAIR = 8,
-  FP8BS_TILE_128x192_CLUSTER2_W12 = 9,
-  FP8BS_TILE_256x192_PAIR_W12 = 10,
-  FP8BS_TILE_256x128_PAIR = 11,
-  FP8BS_TILE_256x160_PAIR = 12
+  FP8BS_TILE_256x192_PAIR_W12 = 7
 } fp8bs_tile_shape;
 
 /*
@@ -312,7 +306,7 @@ fp8bs_status fp8bs_quant_per_tensor(const void *x_bf16, int64_t rows,
  *   c: E4M3 [M][N], c_scales: f32 [N/128][M] (the layout of
  *   fp8bs_quant_act_1x128's output, so c can feed the next GEMM as its A).
  *   Requires N % 128 == 0 (and the fp8bs_gemm requirements); always uses
- *   128 x 256 output tiles.
+ *   256 x 256 CTA-pair tiles.
  */
 fp8bs_status fp8bs_gemm_quant_out(const uint8_t *a, const float *sa,
                                   const uint8_t *b, const float *sb,

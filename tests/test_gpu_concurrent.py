@@ -14,7 +14,7 @@ from tests._helpers import assert_codes_equal, assert_gemm_f32, dev, dev_bf16, h
 pytestmark = pytest.mark.gpu
 
 BLOCK = 0
-TILE_256x160_PAIR = 12
+TILE_256x160_PAIR = 3
 
 
 def test_two_threads_two_streams(fp8bs, oracle_mod):

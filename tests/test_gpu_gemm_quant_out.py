@@ -3,7 +3,7 @@
 once more to be quantized; page P1, paragraph 3: the 1x128 rule).
 
 The fused kernel computes the same FP32 sums as the FP32-output GEMM of the
-same tile shape (128 x 256, cluster of 2), so its codes and scales must equal,
+same tile shape (the 256 x 256 CTA pair), so its codes and scales must equal,
 bit for bit, the oracle's 1x128 quantizer applied to that kernel's own FP32
 output.  Separately, the dequantized result is compared with the oracle's
 double-precision GEMM: each element within half an E4M3 step of it (plus the
@@ -18,7 +18,7 @@ from tests._helpers import assert_codes_equal, assert_scales_equal, dev, host
 pytestmark = pytest.mark.gpu
 
 BLOCK, TILE = 0, 1
-TILE_128x256 = 2
+TILE_256x256_PAIR = 6
 
 
 def _inputs(oracle_mod, M, N, K, seed, bkind):
@@ -40,7 +40,7 @@ def _check(fp8bs, oracle_mod, a, sa, b, sb, bkind, what, ref=None):
     cs = torch.full((N // 128, M), float("nan"), dtype=torch.float32, device="cuda")
     fp8bs.gemm_quant_out(da, dsa, db, dsb, bkind, out=c, out_scales=cs)
     c32 = host(fp8bs.gemm(da, dsa, db, dsb, bkind, out_dtype=torch.float32,
-                          tile=TILE_128x256))
+                          tile=TILE_256x256_PAIR))
     torch.cuda.synchronize()
     q_ref, s_ref = oracle_mod.quant_f32_1x128(c32)
     assert_codes_equal(c, q_ref, what + " codes")
