@@ -12,6 +12,7 @@
 namespace {
 
 thread_local int t_last_cuda_error = 0;
+thread_local unsigned int* t_err_words = nullptr;  // see fp8bs_get_device_error
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -285,14 +286,30 @@ const char* fp8bs_status_string(fp8bs_status s) {
 }
 
 fp8bs_status fp8bs_get_device_error(fp8bs_stream_t stream) {
-  cudaError_t e = cudaStreamSynchronize(as_cuda(stream));
+  // Two mapped pinned host words per calling host thread, allocated on its
+  // first query and kept until the process exits.  The device writes the
+  // taken error words there in stream order; the host reads them after the
+  // stream synchronization.
+  if (!t_err_words) {
+    void* p = nullptr;
+    cudaError_t e =
+        cudaHostAlloc(&p, 2 * sizeof(unsigned int), cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) return cuda_status(e);
+    t_err_words = static_cast<unsigned int*>(p);
+  }
+  volatile unsigned int* w = t_err_words;
+  w[0] = 0u;
+  w[1] = 0u;
+  unsigned int* dptr = nullptr;
+  cudaError_t e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&dptr), t_err_words, 0);
   if (e != cudaSuccess) return cuda_status(e);
-  unsigned int g = 0, q = 0;
-  e = fp8bs::read_and_clear_gemm_error(&g);
+  e = fp8bs::enqueue_take_gemm_error(dptr, as_cuda(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  e = fp8bs::read_and_clear_quant_error(&q);
+  e = fp8bs::enqueue_take_quant_error(dptr + 1, as_cuda(stream));
   if (e != cudaSuccess) return cuda_status(e);
-  return (g | q) ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
+  e = cudaStreamSynchronize(as_cuda(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  return (w[0] | w[1]) ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
 }
 
 int fp8bs_last_cuda_error(void) { return t_last_cuda_error; }

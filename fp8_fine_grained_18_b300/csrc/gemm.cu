@@ -955,18 +955,16 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   return g.promote ? launch_out<true>(g, stream) : launch_out<false>(g, stream);
 }
 
-cudaError_t read_and_clear_gemm_error(unsigned int* word) {
-  *word = 0;
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
-  if (e != cudaSuccess) return e;
-  if (v) {
-    const unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
-    if (e != cudaSuccess) return e;
-  }
-  *word = v;
-  return cudaSuccess;
+// Moves the error word into *dst and clears it in one atomic step, in
+// stream order: an error set by any kernel on the device is taken by exactly
+// one query.
+__global__ void take_gemm_error_kernel(unsigned int* dst) {
+  *dst = atomicExch(&g_device_error, 0u);
+}
+
+cudaError_t enqueue_take_gemm_error(unsigned int* dst, cudaStream_t stream) {
+  take_gemm_error_kernel<<<1, 1, 0, stream>>>(dst);
+  return cudaGetLastError();
 }
 
 }  // namespace fp8bs

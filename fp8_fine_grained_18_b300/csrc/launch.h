@@ -58,10 +58,11 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
-// Read and clear the device error words of the bounded waits in the GEMM
-// and in the quantizers (the caller synchronizes first).  *word = 0 when
-// nothing timed out.
-cudaError_t read_and_clear_gemm_error(unsigned int* word);
-cudaError_t read_and_clear_quant_error(unsigned int* word);
+// Enqueue on `stream` a one-thread kernel that atomically exchanges the
+// device error word of the bounded waits in the GEMM (or in the quantizers)
+// with 0 and writes the old value to *dst (device-visible memory, e.g. a
+// mapped pinned host word).  0 means nothing timed out.
+cudaError_t enqueue_take_gemm_error(unsigned int* dst, cudaStream_t stream);
+cudaError_t enqueue_take_quant_error(unsigned int* dst, cudaStream_t stream);
 
 }  // namespace fp8bs

@@ -1050,18 +1050,14 @@ cudaError_t launch_requant_e5m6_to_128x1(const uint8_t* e5, const float* s5, int
   return cudaGetLastError();
 }
 
-cudaError_t read_and_clear_quant_error(unsigned int* word) {
-  *word = 0;
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(v));
-  if (e != cudaSuccess) return e;
-  if (v) {
-    const unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(zero));
-    if (e != cudaSuccess) return e;
-  }
-  *word = v;
-  return cudaSuccess;
+// The quantizers' error word, taken like the GEMM's (enqueue_take_gemm_error).
+__global__ void take_quant_error_kernel(unsigned int* dst) {
+  *dst = atomicExch(&g_quant_error, 0u);
+}
+
+cudaError_t enqueue_take_quant_error(unsigned int* dst, cudaStream_t stream) {
+  take_quant_error_kernel<<<1, 1, 0, stream>>>(dst);
+  return cudaGetLastError();
 }
 
 }  // namespace fp8bs

@@ -318,9 +318,16 @@ fp8bs_status fp8bs_gemm_quant_out(const uint8_t *a, const float *sa,
 const char *fp8bs_status_string(fp8bs_status status);
 
 /*
- * Synchronizes `stream`, then reports and clears the device error word that
- * bounded waits inside the GEMM set when they give up (FP8BS_ERR_TIMEOUT),
- * or FP8BS_ERR_CUDA if the synchronization itself failed.
+ * Reports and clears the device error words that bounded waits inside the
+ * kernels set when they give up (FP8BS_ERR_TIMEOUT), or FP8BS_ERR_CUDA if a
+ * CUDA call failed.  The words are per device and shared by every stream and
+ * host thread: a kernel that timed out on any stream sets them.  The query
+ * takes them in stream order on `stream` with an atomic exchange (one
+ * one-thread kernel per word), then synchronizes `stream`, so each timeout
+ * is reported by exactly one query and none is lost.  To attribute a
+ * timeout to one stream, query after a device-wide synchronization.  The
+ * first query from a host thread allocates two mapped pinned host words for
+ * that thread, kept until the process exits.
  */
 fp8bs_status fp8bs_get_device_error(fp8bs_stream_t stream);
 

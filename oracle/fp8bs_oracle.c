@@ -465,7 +465,7 @@ void fp8bs_oracle_gemm_limited_acc(const uint8_t *a, const float *sa,
   for (int64_t i = 0; i < count; ++i) {
     int64_t m = ms[i], n = ns[i];
     double acc = 0.0;   /* the modelled tensor-core accumulator */
-    double total = 0.0; /* the promoted FP32-side sum */
+    double total = 0.0; /* the promoted sum, kept in double */
     for (int64_t k0 = 0; k0 < K; k0 += group) {
       /* [P2¶3] align the group's products and the running sum to the
        * largest exponent, keep `bits` bits below it (sign-fill right shift

@@ -173,9 +173,11 @@ void fp8bs_oracle_gemm_sampled(const uint8_t *a, const float *sa,
  * Every group of `group` products and the running sum are aligned to the
  * largest exponent among them, each truncated (two's-complement, toward
  * -inf) to a multiple of 2^(E-bits+1), summed exactly and truncated toward
- * zero back to FP32.  With promote_every > 0 the accumulator is added into
- * an exact FP32 sum (RN) every promote_every products and reset, with the
- * scales applied at that point; with promote_every == 0 the whole K is
+ * zero back to FP32.  With promote_every > 0 the accumulator, times its
+ * K-group's scales, is added into a double-precision sum every
+ * promote_every products and reset (the model keeps the promoted side
+ * exact, so only the limited accumulator loses precision); with
+ * promote_every == 0 the whole K is
  * accumulated this way and the scales of K-group 0 are applied once at the
  * end (row-wise codes).  Computes a list of (m, n) outputs. */
 void fp8bs_oracle_gemm_limited_acc(const uint8_t *a, const float *sa,

@@ -221,8 +221,21 @@ def test_backward_quantizers_full(fp8bs, oracle_mod):
     # weight with transposed copy (input-gradient B operand)
     q, s, qT2, sT2 = fp8bs.quant_weight_128x128(dev_bf16(inp["W"]), transposed=True)
     rq, rs, rqT2, rsT2 = oracle_mod.quant_weight_128x128(inp["W"], transposed=True)
+    assert_codes_equal(q, rq, "W codes (transposed call)")
+    assert_scales_equal(s, rs, "W scales (transposed call)")
     assert_codes_equal(qT2, rqT2, "W^T codes")
     assert_scales_equal(sT2, rsT2, "W^T scales")
+
+
+def test_stress_activation_full(fp8bs, oracle_mod):
+    """Q1 on the large-K stress operand A (8192 x 16384, rows U(-1, 1) x
+    10^U(-2, 2)), the bench step's first quantizer launch: every code and
+    scale."""
+    inp = synth.make_inputs("stress")
+    q, s = fp8bs.quant_act_1x128(dev_bf16(inp["A"]))
+    rq, rs = oracle_mod.quant_act_1x128(inp["A"])
+    assert_codes_equal(q, rq, "stress A codes")
+    assert_scales_equal(s, rs, "stress A scales")
 
 
 def test_hand_worked_tiles_on_gpu(fp8bs):
