@@ -1,23 +1,27 @@
 #!/usr/bin/env python3
-"""Benchmark of the fine-grained FP8 forward path on B300.
+"""Benchmark of the fine-grained FP8 path on B300.
 
-One step = one pass of the path over one batch of the dense workload
-(attention-projection shape: M = 4096 tokens, N = K = 7168; activations
-N(0,1) with 0.1% outlier channels x100, weights N(0,0.02); bf16 in, bf16
-out): quantize the activations in 1x128 tiles and the weights in 128x128
-blocks (one launch), then the block-scaled FP8 GEMM with FP32 promotion.
-With `--rows 1` (the default) every other hot-path operation is also timed
-at its own workload shape and reported under `rows`.
+One step = one pass of the path over one batch of the large-K stress
+workload (M = N = 8192, K = 16384; both operands U(-1, 1) with per-row
+magnitudes 10^U(-2, 2), bf16 in, FP32 out): quantize A and B in 1x128 tiles
+(two launches), then the block-scaled FP8 GEMM with FP32 promotion every
+128 K (B scales per 1x128 tile of each B row).  This is the largest of the
+workloads, the one the throughput targets are set on.  With `--rows 1` (the
+default) every other hot-path operation is also timed at its own workload
+shape and at the 8192 x 16384 bandwidth shape, and reported under `rows`,
+each with the SM clock sampled while it ran.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Prints one JSON line.  `value` is whole-job TFLOP/s (2*M*N*K per step per
 GPU) with inputs resident in HBM, CUDA-event timed on the launching stream,
-L2 flushed between steps; `e2e` is the same metric through the C ABI from
-pinned host buffers (host<->device copies inside the timed region).  Under
-torchrun every rank runs its own replica (weak scaling; no collective on the
-data path) and the slowest rank's time is used.  `--impl reference` times the
-CPU oracle on a bounded sample of the same workload.
+L2 flushed between steps (the inputs, 268 MB each, are larger than L2
+anyway); `e2e` is the same metric through the C ABI from pinned host
+buffers (host<->device copies of both operands and of C inside the timed
+region).  Under torchrun every rank runs its own replica (weak scaling; no
+collective on the data path) and the slowest rank's time is used.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload.
 """
 import argparse
 import hashlib
@@ -35,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-WORKLOAD = "dense"
+WORKLOAD = "stress"
 METRIC = ("block-scaled FP8 GEMM TFLOP/s and % dense FP8 peak; "
           "quantizer GB/s and % HBM peak")
 # Dense FP8 peak = measured bf16 peak x the nominal fp8/bf16 ratio (4.5/2.25).
@@ -235,6 +239,10 @@ def algorithmic_bytes_q3(M, K):
     return M * K * 2 + 2 * 4 * M * (K // 128)
 
 
+def _bf16_dev(torch, bits, dev):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -259,17 +267,22 @@ def run_ours(args):
     qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
     sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
     qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
-    sb = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
-    c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    sb = torch.empty((K // 128, N), dtype=torch.float32, device=dev)
+    c = torch.empty((M, N), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
+    tile = fp8bs.BSCALE_TILE_1x128
 
-    def step():
-        fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb)
-        fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=c)
+    def quantize():
+        fp8bs.quant_act_1x128(a, q=qa, scales=sa)
+        fp8bs.quant_act_1x128(b, q=qb, scales=sb)
+
+    def gemm():
+        fp8bs.gemm(qa, sa, qb, sb, tile, out_dtype=torch.float32, out=c)
 
     for _ in range(args.warmup):
-        step()
+        quantize()
+        gemm()
     torch.cuda.synchronize()
     if fp8bs.get_device_error(dev) != fp8bs.OK:
         raise RuntimeError("device error during warm-up")
@@ -285,9 +298,9 @@ def run_ours(args):
             flush.zero_()
             e = ev[i]
             e[0].record(stream)
-            fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb)
+            quantize()
             e[1].record(stream)
-            fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=c)
+            gemm()
             e[2].record(stream)
         torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -311,7 +324,8 @@ def run_ours(args):
     tr = TRAFFIC.get("gemm")
     if tr and tr.get("src_sha") == kernel_source_sha():
         traffic = tr["bytes"]
-    roofline = {"bound": "tensor", "kernel": "gemm (block-scaled FP8, promoted)",
+    roofline = {"bound": "tensor", "kernel": "gemm (block-scaled FP8, promoted every 128 K, "
+                                             "1x128 B scales, FP32 out)",
                 "achieved": round(g_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(g_tflops / fp8_peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} "
@@ -319,21 +333,19 @@ def run_ours(args):
                 "frac_of_sustained": round(g_tflops / (peaks["bf16_tflops_sustained"] * FP8_OVER_BF16), 4),
                 "algorithmic_flops_per_launch": flops}
     hbm = peaks["hbm_gbs"]
-    q_gbs = (algorithmic_bytes_q1(M, K) + algorithmic_bytes_q2(N, K)) / \
-        (statistics.mean(t_q) * 1e-3) / 1e9
+    q_gbs = 2 * algorithmic_bytes_q1(M, K) / (statistics.mean(t_q) * 1e-3) / 1e9
     kernels = {
-        "quant_act_and_weight (Q1 of A and Q2 of W, one launch)": {
+        "quant_act_1x128 of A and of B (two launches)": {
             "ms": round(statistics.mean(t_q), 4), "GB/s": round(q_gbs, 1),
             "frac_hbm": round(q_gbs / hbm, 4), "frac_hbm_nominal_8TBs": round(q_gbs / HBM_NOMINAL_GBS, 4)},
         "gemm": {"ms": round(g_ms, 4), "TFLOP/s": round(g_tflops, 1),
                  "frac_fp8_peak": round(g_tflops / fp8_peak, 4)},
     }
+    del flush
 
     # End to end through the C ABI from pinned host buffers: every step
-    # copies its inputs host->device, runs the path and reads the result
-    # back.  Two buffer sets and two copy streams (one per direction) let the
-    # copies of neighbouring steps overlap the compute of the current one.
-    e2e = measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, max(3, min(args.steps, 20)))
+    # copies both operands host->device, runs the path and reads C back.
+    e2e = measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, max(3, min(args.steps, 10)))
     e2e_ms = max_over_ranks(e2e.pop("_ms"), dist, dev)
     e2e["value"] = round(whole_job_rate(flops, world, 1, e2e_ms) / 1e12, 2)
     e2e["ms_per_step"] = round(e2e_ms, 3)
@@ -343,19 +355,23 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": "dense attention-projection Fprop: quantize A 1x128 + W 128x128, "
-                               "block-scaled FP8 GEMM, bf16 out",
+        "config": {"workload": "large-K accumulation stress Fprop: quantize A and B 1x128, "
+                               "block-scaled FP8 GEMM promoted every 128 K, FP32 out",
                    "M": M, "N": N, "K": K, "seed": w.seed,
-                   "l2": "flushed between steps (256 MB write, outside the timed events)",
+                   "inputs": "A, B U(-1,1) rows x 10^U(-2,2), bf16",
+                   "l2": "flushed between steps (256 MB write, outside the timed events); "
+                         "inputs 268 MB each, larger than L2",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline, "kernels": kernels, "e2e": e2e,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(), "wall_timed_s": round(wall, 4),
     }
+    del a, b, qa, sa, qb, sb, c
+    torch.cuda.empty_cache()
     # the per-row details are a single-GPU measurement: under torchrun they
     # would hold every GPU while rank 0 alone runs them
     if args.rows and world == 1:
-        out["rows"] = measure_rows(fp8bs, torch, dev, peaks)
+        out["rows"] = measure_rows(fp8bs, torch, dev, peaks, local_rank)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(M, N, K, inp, budget_s=20.0)
     if world > 1:
@@ -366,11 +382,11 @@ def run_ours(args):
 
 
 def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
-    """Per-step time of the forward path with host<->device copies inside:
-    step i copies A and W from pinned host memory (stream h2d), quantizes
-    both and multiplies (stream comp), and copies C back to pinned host
-    memory (stream d2h).  Buffer set i % 2 is reused by step i + 2 only
-    after step i's read-back finished."""
+    """Per-step time of the path with host<->device copies inside: step i
+    copies A and B from pinned host memory (two copy streams), quantizes both
+    and multiplies (stream comp), and copies C back to pinned host memory
+    (stream d2h).  Both operands are sent again every step.  Buffer set
+    i % 2 is reused by step i + 2 only after step i's read-back finished."""
     a_pin, b_pin = a_host.pin_memory(), b_host.pin_memory()
     sets = []
     for _ in range(2):
@@ -380,12 +396,12 @@ def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
             "qa": torch.empty((M, K), dtype=torch.uint8, device=dev),
             "sa": torch.empty((K // 128, M), dtype=torch.float32, device=dev),
             "qb": torch.empty((N, K), dtype=torch.uint8, device=dev),
-            "sb": torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
-            "c": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
-            "c_pin": torch.empty((M, N), dtype=torch.bfloat16).pin_memory(),
+            "sb": torch.empty((K // 128, N), dtype=torch.float32, device=dev),
+            "c": torch.empty((M, N), dtype=torch.float32, device=dev),
+            "c_pin": torch.empty((M, N), dtype=torch.float32).pin_memory(),
         })
     h2d, comp, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    h2d_w = torch.cuda.Stream(dev)  # W's copy beside A's, on a second copy engine
+    h2d_b = torch.cuda.Stream(dev)  # B's copy beside A's, on a second copy engine
     ev = lambda: torch.cuda.Event()  # noqa: E731
 
     def run(n):
@@ -398,20 +414,20 @@ def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
                     h2d.wait_event(done[k])  # step i-2 finished reading a/b of this set
                 st["a"].copy_(a_pin, non_blocking=True)
                 loaded[k] = ev(); loaded[k].record(h2d)
-            with torch.cuda.stream(h2d_w):
+            with torch.cuda.stream(h2d_b):
                 if done[k] is not None:
-                    h2d_w.wait_event(done[k])
+                    h2d_b.wait_event(done[k])
                 st["b"].copy_(b_pin, non_blocking=True)
-                loaded_w = ev(); loaded_w.record(h2d_w)
+                loaded_b = ev(); loaded_b.record(h2d_b)
             with torch.cuda.stream(comp):
                 comp.wait_event(loaded[k])
-                comp.wait_event(loaded_w)
+                comp.wait_event(loaded_b)
                 if read[k] is not None:
                     comp.wait_event(read[k])  # step i-2's result has been read back
-                fp8bs.quant_act_and_weight(st["a"], st["b"], q=st["qa"], scales=st["sa"],
-                                           qw=st["qb"], w_scales=st["sb"])
-                fp8bs.gemm(st["qa"], st["sa"], st["qb"], st["sb"], fp8bs.BSCALE_BLOCK_128x128,
-                           out_dtype=torch.bfloat16, out=st["c"])
+                fp8bs.quant_act_1x128(st["a"], q=st["qa"], scales=st["sa"])
+                fp8bs.quant_act_1x128(st["b"], q=st["qb"], scales=st["sb"])
+                fp8bs.gemm(st["qa"], st["sa"], st["qb"], st["sb"], fp8bs.BSCALE_TILE_1x128,
+                           out_dtype=torch.float32, out=st["c"])
                 done[k] = ev(); done[k].record(comp)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(done[k])
@@ -423,39 +439,90 @@ def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(h2d)
-    h2d_w.wait_event(e0)  # nothing of the timed steps starts before e0
+    h2d_b.wait_event(e0)  # nothing of the timed steps starts before e0
     read = run(steps)
     main = torch.cuda.current_stream(dev)
     for r in read:
         main.wait_event(r)
     e1.record(main)
     torch.cuda.synchronize(dev)
-    return {"unit": "TFLOP/s", "h2d_bytes_per_step": (M * K + N * K) * 2,
-            "d2h_bytes_per_step": M * N * 2, "_ms": e0.elapsed_time(e1) / steps,
-            "pipelining": "2 buffer sets; H2D of A, H2D of W, compute and D2H on separate streams"}
+    out = {"unit": "TFLOP/s", "h2d_bytes_per_step": (M * K + N * K) * 2,
+           "d2h_bytes_per_step": M * N * 4, "_ms": e0.elapsed_time(e1) / steps,
+           "pipelining": "2 buffer sets; both operands sent host->device every step (A and B on "
+                         "two copy streams), compute and the read-back of C on separate streams"}
+    del sets, a_pin, b_pin
+    torch.cuda.empty_cache()
+    return out
 
 
-def _time_ms(fn, torch, iters=10, flush=None):
+def _time_ms(fn, torch, flush, min_ms=60.0, min_iters=10, max_iters=2000):
+    """Median CUDA-event time of fn() with L2 flushed before each launch.
+    The iterations are queued without a host synchronization in between, so
+    each launch is already queued behind its flush when its start event is
+    reached (no host launch gap inside the timed events).  It runs at least
+    min_iters times and about min_ms of device time in all, so that the
+    clock sampler around it sees several samples."""
     stream = torch.cuda.current_stream()
-    ts = []
-    for _ in range(iters):
-        if flush is not None:
+
+    def batch(n):
+        evs = []
+        for _ in range(n):
             flush.zero_()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        fn()
-        e.record(stream)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            fn()
+            e.record(stream)
+            evs.append((s, e))
         torch.cuda.synchronize()
-        ts.append(s.elapsed_time(e))
-    return statistics.median(ts)
+        return evs
+
+    t0 = time.perf_counter()
+    batch(3)
+    per_iter_ms = (time.perf_counter() - t0) * 1e3 / 3
+    n = int(min(max_iters, max(min_iters, min_ms / max(per_iter_ms, 1e-3))))
+    evs = batch(n)
+    ts = [s.elapsed_time(e) for s, e in evs]
+    return statistics.median(ts), len(ts)
 
 
-def measure_rows(fp8bs, torch, dev, peaks):
-    """Every hot-path row at its own workload: quantizer GB/s, GEMM TFLOP/s."""
+def _clock_brief(sampler):
+    sm = sampler.summary()
+    return {"sm_mhz": sm["sm_mhz"], "samples": sm["samples"], "reasons": sm["reasons"]}
+
+
+def measure_rows(fp8bs, torch, dev, peaks, index):
+    """Every hot-path row at its own workload, and every quantizer at the
+    8192 x 16384 bandwidth shape: quantizer GB/s, GEMM TFLOP/s; each row with
+    the SM clock sampled while it ran."""
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     rows = {}
+
+    def timed(fn):
+        with ClockSampler(index) as smp:
+            ms, n = _time_ms(fn, torch, flush)
+        return ms, n, _clock_brief(smp)
+
+    def gemm_row(name, qa, sa, qb, sb, bkind, out_dtype, promote=True):
+        M, K = qa.shape
+        N = qb.shape[0]
+        c = torch.empty((M, N), dtype=out_dtype, device=dev)
+        ms, n, clk = timed(lambda: fp8bs.gemm(qa, sa, qb, sb, bkind, out_dtype=out_dtype, out=c,
+                                              promote=promote))
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        rows[name] = {"M": M, "N": N, "K": K, "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                      "frac_fp8_peak": round(tf / fp8_peak, 4), "launches": n, "clocks": clk}
+
+    def quant_row(name, fn, nbytes):
+        ms, n, clk = timed(fn)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                      "frac_hbm_nominal_8TBs": round(gbs / HBM_NOMINAL_GBS, 4), "launches": n,
+                      "clocks": clk}
+
+    def bf(x):
+        return _bf16_dev(torch, x, dev)
 
     # Context only: the library's own FP8 GEMM (cuBLASLt through
     # torch._scaled_mm, one scale per tensor, no fine-grained scales and no
@@ -465,96 +532,75 @@ def measure_rows(fp8bs, torch, dev, peaks):
         x8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
         y8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
         one = torch.ones((), device=dev)
-        ms = _time_ms(lambda: torch._scaled_mm(x8, y8, scale_a=one, scale_b=one,
-                                               out_dtype=torch.bfloat16), torch, flush=flush)
+        ms, _, clk = timed(lambda: torch._scaled_mm(x8, y8, scale_a=one, scale_b=one,
+                                                    out_dtype=torch.bfloat16))
         rows["context: library FP8 GEMM (per-tensor scales) 8192^3 bf16"] = {
-            "ms": round(ms, 4), "TFLOP/s": round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1)}
+            "ms": round(ms, 4), "TFLOP/s": round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1),
+            "clocks": clk}
         del x8, y8
     except Exception as e:  # noqa: BLE001 -- context only
         rows["context: library FP8 GEMM (per-tensor scales) 8192^3 bf16"] = {"error": str(e)[:120]}
 
-    def bf(x):
-        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    def gemm_row(name, qa, sa, qb, sb, bkind, out_dtype, promote=True):
-        M, K = qa.shape
-        N = qb.shape[0]
-        c = torch.empty((M, N), dtype=out_dtype, device=dev)
-        ms = _time_ms(lambda: fp8bs.gemm(qa, sa, qb, sb, bkind, out_dtype=out_dtype, out=c,
-                                         promote=promote), torch, flush=flush)
-        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-        rows[name] = {"M": M, "N": N, "K": K, "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                      "frac_fp8_peak": round(tf / fp8_peak, 4)}
-
-    def quant_row(name, fn, nbytes):
-        ms = _time_ms(fn, torch, flush=flush)
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
-                      "frac_hbm_nominal_8TBs": round(gbs / HBM_NOMINAL_GBS, 4)}
-
-    # the dense step's quantizers as separate launches
+    # the dense attention-projection step: both operands in one quantizer
+    # launch, then the GEMM (bf16 out)
     dense = synth.make_inputs("dense")
     a, b = bf(dense["A"]), bf(dense["B"])
     del dense
-    qa, sa = fp8bs.quant_act_1x128(a)
-    qb, sb = fp8bs.quant_weight_128x128(b)
+    qa, sa, qb, sb = fp8bs.quant_act_and_weight(a, b)
+    cd = torch.empty((4096, 7168), dtype=torch.bfloat16, device=dev)
+
+    def dense_step():
+        fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb)
+        fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=cd)
+    ms, n, clk = timed(dense_step)
+    tf = 2.0 * 4096 * 7168 * 7168 / (ms * 1e-3) / 1e12
+    rows["dense step 4096x7168x7168: Q1 of A + Q2 of W (one launch), G1 bf16"] = {
+        "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "launches": n, "clocks": clk}
+    quant_row("Q1+Q2 dense A 4096x7168 + W 7168x7168 (one launch)",
+              lambda: fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb),
+              algorithmic_bytes_q1(4096, 7168) + algorithmic_bytes_q2(7168, 7168))
+    gemm_row("G1 dense 4096x7168x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
     quant_row("Q1 dense A 4096x7168 (own launch)", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
               algorithmic_bytes_q1(4096, 7168))
     quant_row("Q2 dense W 7168x7168 (own launch)",
               lambda: fp8bs.quant_weight_128x128(b, q=qb, scales=sb), algorithmic_bytes_q2(7168, 7168))
-    del a, b, qa, sa, qb, sb
+    del a, b, qa, sa, qb, sb, cd
 
     # MoE up/gate shape
     moe = synth.make_inputs("moe")
     a, b = bf(moe["A"]), bf(moe["B"])
+    del moe
     qa, sa = fp8bs.quant_act_1x128(a)
     qb, sb = fp8bs.quant_weight_128x128(b)
     quant_row("Q1 moe A 8192x7168", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
               algorithmic_bytes_q1(8192, 7168))
     gemm_row("G1 moe 8192x4096x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
-    # per-tensor baseline quantizer: a max-abs pass and a quantize pass
-    qpt, spt, _ = fp8bs.quant_per_tensor(a)
-    quant_row("Q per-tensor moe A 8192x7168 (max-abs pass + quantize pass; 3 B/elt algorithmic)",
-              lambda: fp8bs.quant_per_tensor(a, q=qpt, scale=spt), 3 * 8192 * 7168 + 4)
-    del qpt, spt
     # the GEMM output quantized for the next layer: fused epilogue against
     # the BF16 output written to HBM and quantized by Q1 afterwards
     c8, cs8 = fp8bs.gemm_quant_out(qa, sa, qb, sb, 0)
-    ms_f = _time_ms(lambda: fp8bs.gemm_quant_out(qa, sa, qb, sb, 0, out=c8, out_scales=cs8),
-                    torch, flush=flush)
+    ms_f, n, clk = timed(lambda: fp8bs.gemm_quant_out(qa, sa, qb, sb, 0, out=c8, out_scales=cs8))
     cbf = torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev)
     qc, sc = fp8bs.quant_act_1x128(cbf)
 
     def unfused():
         fp8bs.gemm(qa, sa, qb, sb, 0, out_dtype=torch.bfloat16, out=cbf)
         fp8bs.quant_act_1x128(cbf, q=qc, scales=sc)
-    ms_u = _time_ms(unfused, torch, flush=flush)
+    ms_u, _, _ = timed(unfused)
     tflop = 2.0 * 8192 * 4096 * 7168 / 1e12
     rows["G1+Q moe 8192x4096x7168, output quantized 1x128 in the epilogue"] = {
         "ms": round(ms_f, 4), "TFLOP/s": round(tflop / (ms_f * 1e-3), 1),
         "frac_fp8_peak": round(tflop / (ms_f * 1e-3) / fp8_peak, 4),
-        "unfused_gemm_bf16_then_Q1_ms": round(ms_u, 4)}
+        "unfused_gemm_bf16_then_Q1_ms": round(ms_u, 4), "launches": n, "clocks": clk}
     del a, b, qa, sa, qb, sb, c8, cs8, cbf, qc, sc
 
-    # backward chain
+    # backward chain at its own shapes
     bwd = synth.make_inputs("bwd")
     x, wt, dy = bf(bwd["X"]), bf(bwd["W"]), bf(bwd["dY"])
+    del bwd
     qx, sx = fp8bs.quant_act_1x128(x)
     qxT, sxT = fp8bs.requant_1x128_to_128x1(qx, sx)
     quant_row("Q3 requant X 4096x2048", lambda: fp8bs.requant_1x128_to_128x1(qx, sx, qT=qxT, scalesT=sxT),
               algorithmic_bytes_q3(4096, 2048))
-    # E5M6 cache of X: with the forward E4M3 codes from the same read, and
-    # re-tiled into the Wgrad operand
-    e5 = fp8bs.quant_act_e5m6(x)
-    n_x = 4096 * 2048
-    quant_row("Q1+E5M6 X 4096x2048 (E4M3 codes and E5M6 cache, one read)",
-              lambda: fp8bs.quant_act_e5m6(x, packed=e5[0], scales=e5[1], q=e5[2], q_scales=e5[3]),
-              int(n_x * (2 + 1 + 1.5 + 8 / 128)))
-    q5T, s5T = fp8bs.requant_e5m6_to_128x1(e5[0], e5[1])
-    quant_row("Q3-E5M6 requant X cache 4096x2048 -> 128x1 E4M3",
-              lambda: fp8bs.requant_e5m6_to_128x1(e5[0], e5[1], qT=q5T, scalesT=s5T),
-              int(n_x * (1.5 + 1 + 8 / 128)))
-    del e5, q5T, s5T
     qdyT, sdyT = fp8bs.quant_act_1x128(dy, transpose_out=True)
     quant_row("Q1T dY 4096x7168 (128x1, transposed out)",
               lambda: fp8bs.quant_act_1x128(dy, transpose_out=True, q=qdyT, scales=sdyT),
@@ -572,43 +618,82 @@ def measure_rows(fp8bs, torch, dev, peaks):
     gemm_row("G1 wgrad 7168x2048x4096 f32 (1x128 B scales)", qdyT, sdyT, qxT, sxT, 1, torch.float32)
     del x, wt, dy, qx, sx, qxT, sxT, qdyT, sdyT, qdy, sdy, qw, sw, qwT, swT
 
-    # large-K stress, promoted and un-promoted
+    # every quantizer at the bandwidth shape 8192 x 16384 (the stress A
+    # operand), and the un-promoted GEMM at the stress shape
     st = synth.make_inputs("stress")
     a, b = bf(st["A"]), bf(st["B"])
     del st
+    Mb, Kb = 8192, 16384
+    n_el = Mb * Kb
     qa, sa = fp8bs.quant_act_1x128(a)
     qb, sb = fp8bs.quant_act_1x128(b)
-    quant_row("Q1 stress A 8192x16384", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
-              algorithmic_bytes_q1(8192, 16384))
-    gemm_row("G1 stress 8192x8192x16384 f32", qa, sa, qb, sb, 1, torch.float32)
+    quant_row("Q1 8192x16384", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
+              algorithmic_bytes_q1(Mb, Kb))
     gemm_row("G2 un-promoted stress 8192x8192x16384 f32", qa, sa, qb, sb, 1, torch.float32,
              promote=False)
+    del b, qb, sb
+    qT, sT = fp8bs.quant_act_1x128(a, transpose_out=True)
+    quant_row("Q1T 8192x16384 (128x1, transposed out)",
+              lambda: fp8bs.quant_act_1x128(a, transpose_out=True, q=qT, scales=sT),
+              algorithmic_bytes_q1(Mb, Kb))
+    q2, s2 = torch.empty_like(qa), torch.empty_like(sa)
+    quant_row("Q1+Q1T fused 8192x16384 (both tilings, one read)",
+              lambda: fp8bs.quant_act_dual(a, q2, s2, qT, sT), algorithmic_bytes_dual(Mb, Kb))
+    del q2, s2
+    quant_row("Q3 requant 8192x16384", lambda: fp8bs.requant_1x128_to_128x1(qa, sa, qT=qT, scalesT=sT),
+              algorithmic_bytes_q3(Mb, Kb))
+    qw, sw, qwT, swT = fp8bs.quant_weight_128x128(a, transposed=True)
+    quant_row("Q2 8192x16384", lambda: fp8bs.quant_weight_128x128(a, q=qw, scales=sw),
+              algorithmic_bytes_q2(Mb, Kb))
+    quant_row("Q2+T 8192x16384 (with transposed copy)",
+              lambda: fp8bs.quant_weight_128x128(a, transposed=True, q=qw, scales=sw, qT=qwT, scalesT=swT),
+              algorithmic_bytes_q2(Mb, Kb, transposed=True))
+    del qw, sw, qwT, swT
+    e5 = fp8bs.quant_act_e5m6(a)
+    quant_row("Q1+E5M6 8192x16384 (E4M3 codes and E5M6 cache, one read)",
+              lambda: fp8bs.quant_act_e5m6(a, packed=e5[0], scales=e5[1], q=e5[2], q_scales=e5[3]),
+              int(n_el * (2 + 1 + 1.5 + 8 / 128)))
+    quant_row("Q3-E5M6 requant 8192x16384 cache -> 128x1 E4M3",
+              lambda: fp8bs.requant_e5m6_to_128x1(e5[0], e5[1], qT=qT, scalesT=sT),
+              int(n_el * (1.5 + 1 + 8 / 128)))
+    del e5
+    qpt, spt, _ = fp8bs.quant_per_tensor(a)
+    quant_row("Q per-tensor 8192x16384 (max-abs pass + quantize pass; 3 B/elt algorithmic)",
+              lambda: fp8bs.quant_per_tensor(a, q=qpt, scale=spt), 3 * n_el + 4)
+    del a, qa, sa, qT, sT, qpt, spt, flush
+    torch.cuda.empty_cache()
     return rows
 
 
 def cpu_baseline(M, N, K, inp, budget_s=20.0):
-    """The oracle, as it stands, on a bounded sample of the step's workload."""
+    """The oracle, as it stands, on a bounded sample of the step's workload:
+    quantize a few rows of A and of B (1x128) and compute their GEMM block
+    in double."""
     import oracle
     oracle.lib()
-    m_s = 32
-    w_rows = 128
+    m_s, n_s = 8, 256
     t0 = time.perf_counter()
     qa, sa = oracle.quant_act_1x128(inp["A"][:m_s])
-    qw_part, _ = oracle.quant_weight_128x128(inp["B"][:w_rows])
-    t1 = time.perf_counter()
-    # GEMM rows need the full quantized weight; its quantization is counted
-    # above only for the sampled share (w_rows of N rows)
-    qw, sw = oracle.quant_weight_128x128(inp["B"])
-    t2 = time.perf_counter()
-    ms = np.repeat(np.arange(m_s), N)
-    ns = np.tile(np.arange(N), m_s)
-    oracle.gemm_sampled(qa, sa, qw, sw, oracle.BSCALE_BLOCK_128x128, ms, ns)
-    t3 = time.perf_counter()
-    secs = (t1 - t0) + (t3 - t2)
-    return {"value": round(2.0 * m_s * N * K / secs / 1e12, 6), "unit": "TFLOP/s",
+    qb, sb = oracle.quant_act_1x128(inp["B"][:n_s])
+    ms = np.repeat(np.arange(m_s), n_s)
+    ns = np.tile(np.arange(n_s), m_s)
+    oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_TILE_1x128, ms, ns)
+    secs = time.perf_counter() - t0
+    # scale the sample to the budget: repeat while it is short
+    reps = max(1, int(budget_s / max(secs, 1e-3) * 0.5))
+    reps = min(reps, 64)
+    t0 = time.perf_counter()
+    for r in range(reps):
+        r0 = (r * m_s) % (M - m_s)
+        qa, sa = oracle.quant_act_1x128(inp["A"][r0:r0 + m_s])
+        qb, sb = oracle.quant_act_1x128(inp["B"][r0:r0 + n_s])
+        oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_TILE_1x128, ms, ns)
+    secs = time.perf_counter() - t0
+    flops = 2.0 * m_s * n_s * K * reps
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{m_s} of {M} activation rows: quantize them (1x128), quantize {w_rows} of "
-                      f"{N} weight rows (128x128), and the {m_s}x{N}x{K} GEMM in double "
+            "sample": f"{reps} repetitions of: quantize {m_s} rows of A and {n_s} rows of B "
+                      f"(1x128 tiles, K = {K}) and their {m_s}x{n_s}x{K} GEMM block in double "
                       f"({secs:.1f} s of CPU time)"}
 
 
@@ -624,28 +709,27 @@ def run_reference(args):
     w = synth.WORKLOADS[WORKLOAD]
     M, N, K = w.M, w.N, w.K
     inp = synth.make_inputs(WORKLOAD)
-    qw, sw = oracle.quant_weight_128x128(inp["B"])
     # size one step so that warm-up + steps take about 90 s in total
-    probe_rows = 2
+    n_s = 256
     t0 = time.perf_counter()
-    _ref_step(oracle, inp, qw, sw, 0, probe_rows, N, K)
-    per_row = (time.perf_counter() - t0) / probe_rows
+    _ref_step(oracle, inp, 0, 2, n_s, K)
+    per_row = (time.perf_counter() - t0) / 2
     budget = 90.0 / max(1, args.steps + args.warmup)
-    rows = int(max(1, min(M, budget / max(per_row, 1e-9))))
+    rows = int(max(1, min(M - 1, budget / max(per_row, 1e-9))))
     for i in range(args.warmup):
-        _ref_step(oracle, inp, qw, sw, i * rows % M, rows, N, K)
+        _ref_step(oracle, inp, (i * rows) % max(1, M - rows), rows, n_s, K)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        _ref_step(oracle, inp, qw, sw, (i * rows) % max(1, M - rows), rows, N, K)
+        _ref_step(oracle, inp, (i * rows) % max(1, M - rows), rows, n_s, K)
     secs = time.perf_counter() - t0
-    value = 2.0 * rows * N * K * args.steps / secs / 1e12
-    sample = (f"each step: {rows} of {M} activation rows quantized (1x128) and their "
-              f"{rows}x{N}x{K} GEMM in double against the weight quantized once (128x128)")
+    value = 2.0 * rows * n_s * K * args.steps / secs / 1e12
+    sample = (f"each step: {rows} rows of A and {n_s} rows of B quantized (1x128) and their "
+              f"{rows}x{n_s}x{K} GEMM block in double")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-           "config": {"workload": "dense attention-projection Fprop (CPU oracle sample)",
+           "config": {"workload": "large-K accumulation stress Fprop (CPU oracle sample)",
                       "M": M, "N": N, "K": K, "seed": w.seed},
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
                             "cores": oracle.num_threads(), "sample": sample},
@@ -654,11 +738,13 @@ def run_reference(args):
     print(json.dumps(out))
 
 
-def _ref_step(oracle, inp, qw, sw, r0, rows, N, K):
+def _ref_step(oracle, inp, r0, rows, n_s, K):
     qa, sa = oracle.quant_act_1x128(inp["A"][r0:r0 + rows])
-    ms = np.repeat(np.arange(rows), N)
-    ns = np.tile(np.arange(N), rows)
-    return oracle.gemm_sampled(qa, sa, qw, sw, oracle.BSCALE_BLOCK_128x128, ms, ns)
+    qb, sb = oracle.quant_act_1x128(inp["B"][r0:r0 + n_s] if r0 + n_s <= inp["B"].shape[0]
+                                    else inp["B"][:n_s])
+    ms = np.repeat(np.arange(rows), n_s)
+    ns = np.tile(np.arange(n_s), rows)
+    return oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_TILE_1x128, ms, ns)
 
 
 def main():

@@ -23,7 +23,8 @@ OUT_BF16, OUT_F32, OUT_E4M3_1x128 = 0, 1, 2
 TILE_AUTO, TILE_128x128, TILE_128x256 = -1, 0, 1
 TILE_256x128_PAIR, TILE_256x160_PAIR, TILE_256x192_PAIR = 2, 3, 4
 TILE_256x224_PAIR, TILE_256x256_PAIR, TILE_256x192_PAIR_W12 = 5, 6, 7
-TILES = tuple(range(8))
+TILE_256x256_PAIR_W16, TILE_256x192_PAIR_W16, TILE_256x128_PAIR_W16 = 8, 9, 10
+TILES = tuple(range(11))
 BSCALE_BLOCK_128x128, BSCALE_TILE_1x128 = 0, 1
 GROUP = 128
 

@@ -50,6 +50,13 @@ cudaStream_t as_cuda(fp8bs_stream_t s) { return reinterpret_cast<cudaStream_t>(s
 
 constexpr int64_t kMaxDim = (int64_t)1 << 31;  // kernels index rows with int32
 
+// The transposing quantizers index 128 x 128 tiles, rows, columns and the
+// packed E5M6 row bytes (1.5 K) with int32.
+bool transposed_shape_ok(int64_t M, int64_t K) {
+  return M < ((int64_t)1 << 30) && K < ((int64_t)1 << 30) &&
+         (M / 128) * (K / 128) < ((int64_t)1 << 31);
+}
+
 fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
                          fp8bs_out_dtype out, int promote, int skip_iter, int tile,
@@ -61,7 +68,7 @@ fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, co
     return FP8BS_ERR_INVALID_ARG;
   if (out == FP8BS_OUT_E4M3_1x128 && (promote != 1 || !c_scales)) return FP8BS_ERR_INVALID_ARG;
   if (promote != 0 && promote != 1) return FP8BS_ERR_INVALID_ARG;
-  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_256x192_PAIR_W12) return FP8BS_ERR_INVALID_ARG;
+  if (tile < FP8BS_TILE_AUTO || tile > FP8BS_TILE_256x128_PAIR_W16) return FP8BS_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FP8BS_OK;
   if (!a || !sa || !b || !sb || !c) return FP8BS_ERR_INVALID_ARG;
   if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
@@ -100,8 +107,8 @@ fp8bs_status fp8bs_quant_act_1x128(const void* x_bf16, int64_t M, int64_t K, int
   if (M == 0 || K == 0) return FP8BS_OK;
   if (!x_bf16 || !q || !scales) return FP8BS_ERR_INVALID_ARG;
   if (K % 128 != 0 || (transpose_out && M % 128 != 0)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (K / 128 > 65535 || (transpose_out && M / 128 > 65535) || M >= kMaxDim)
-    return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (K / 128 > 65535 || M >= kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (transpose_out && !transposed_shape_ok(M, K)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales)) return FP8BS_ERR_MISALIGNED;
   fp8bs_status st = check_device();
   if (st != FP8BS_OK) return st;
@@ -118,7 +125,7 @@ fp8bs_status fp8bs_quant_act_dual(const void* x_bf16, int64_t M, int64_t K, uint
   if (M == 0 || K == 0) return FP8BS_OK;
   if (!x_bf16 || !q || !scales || !qT || !scalesT) return FP8BS_ERR_INVALID_ARG;
   if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (K / 128 > 65535 || M / 128 > 65535) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!transposed_shape_ok(M, K)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(x_bf16) || !aligned16(q) || !aligned16(scales) || !aligned16(qT) ||
       !aligned16(scalesT))
     return FP8BS_ERR_MISALIGNED;
@@ -190,7 +197,7 @@ fp8bs_status fp8bs_requant_e5m6_to_128x1(const uint8_t* packed, const float* sca
   if (M == 0 || K == 0) return FP8BS_OK;
   if (!packed || !scales || !qT || !scalesT) return FP8BS_ERR_INVALID_ARG;
   if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (M / 128 > 65535 || K / 128 > (int64_t)1 << 30) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!transposed_shape_ok(M, K)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(packed) || !aligned16(scales) || !aligned16(qT) || !aligned16(scalesT))
     return FP8BS_ERR_MISALIGNED;
   fp8bs_status st = check_device();
@@ -227,7 +234,7 @@ fp8bs_status fp8bs_requant_1x128_to_128x1(const uint8_t* q, const float* scales,
   if (M == 0 || K == 0) return FP8BS_OK;
   if (!q || !scales || !qT || !scalesT) return FP8BS_ERR_INVALID_ARG;
   if (M % 128 != 0 || K % 128 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
-  if (M / 128 > 65535 || K / 128 > (int64_t)1 << 30) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (!transposed_shape_ok(M, K)) return FP8BS_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(q) || !aligned16(scales) || !aligned16(qT) || !aligned16(scalesT))
     return FP8BS_ERR_MISALIGNED;
   fp8bs_status st = check_device();

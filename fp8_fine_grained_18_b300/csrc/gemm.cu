@@ -118,28 +118,39 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-// PW promotion warps (8 or 12) share the tile's columns: each owns 32 TMEM
-// lanes (rows) and kCols = BN / (PW / 4) columns.
+// PW promotion warps (8, 12 or 16) share the tile's columns: each owns 32
+// TMEM lanes (rows) and kCols = BN / (PW / 4) columns.  Reading the partials
+// out of TMEM is the promotion's bottleneck: one warp's tcgen05.ld calls run
+// one after another (a 32-column load takes about 180 cycles), and the SM's
+// read rate grows with the number of warps reading at once (measured: about
+// 170 B/clk with two warps per SM sub-partition, 310 with four), against
+// 256 B/clk needed to drain one K-group's partial while the tensor cores
+// compute the next at full rate.
 template <int BN, bool PAIR, int PW>
 struct Cfg {
   static constexpr int CM = PAIR ? 2 : 1;  // CTAs per cluster
-  static_assert(PW == 8 || PW == 12, "promotion warps");
+  static_assert(PW == 8 || PW == 12 || PW == 16, "promotion warps");
   static constexpr int kPromoWarps = PW;
   static constexpr int kThreads = 32 * (kFirstPromoWarp + PW);
   static constexpr int kCols = BN / (PW / 4);
   static_assert(kCols % 16 == 0, "columns per promotion warp");
-  // A warp with at most 64 columns reads its whole partial from TMEM at once
-  // and hands the buffer back before its FMAs; wider warps read in steps.
-  static constexpr bool kLoadAll = kCols <= 64;
+  // 16 warps: each reads its steps into one register buffer (the four warps
+  // of a sub-partition overlap one another's reads).  Otherwise a warp with
+  // at most 64 columns reads its whole partial at once and hands the buffer
+  // back before its FMAs, and wider warps read in double-buffered steps.
+  static constexpr bool kSingleBuf = PW == 16;
+  static constexpr bool kLoadAll = !kSingleBuf && kCols <= 64;
   // Register split when the accumulators need more than an even share:
   // warpgroup 0 (producer, MMA, scales) keeps kCtlRegs, the promotion
-  // warpgroups get kPromoRegs.  Their sum must fit in what the launch holds
-  // (65536 registers, kThreads threads).
-  static constexpr bool kRegSplit = PW == 12 || BN > 128;
-  static constexpr int kCtlRegs = PW == 12 ? 56 : 40;
-  static constexpr int kPromoRegs = PW == 12 ? 152 : 232;
+  // warpgroups get kPromoRegs.  Their sum must fit in what the launch holds:
+  // kThreads threads at kLaunchRegs each (65536 / kThreads, rounded down to
+  // the allocation unit of 8).
+  static constexpr bool kRegSplit = PW >= 12 || BN > 128;
+  static constexpr int kCtlRegs = PW == 16 ? 32 : PW == 12 ? 56 : 48;
+  static constexpr int kPromoRegs = PW == 16 ? 112 : PW == 12 ? 152 : 224;
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
   static constexpr int kSplitRegsNeeded = 128 * kCtlRegs + 32 * PW * kPromoRegs;
-  static_assert(!kRegSplit || kSplitRegsNeeded <= 65536, "register split");
+  static_assert(!kRegSplit || kSplitRegsNeeded <= kLaunchRegs * kThreads, "register split");
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   // B rows this CTA loads: the whole B tile, or, for a CTA pair, its own
   // half of the pair's B tile
@@ -173,10 +184,15 @@ struct Cfg {
 template <bool PAIR>
 __device__ __forceinline__ void issue_kgroup(uint32_t d, uint32_t a0, uint32_t b0, uint32_t idesc,
                                              bool accumulate_first) {
+  // Each K = 32 step starts 32 bytes further into the 128-byte rows: +2 in
+  // the descriptor's address field (address >> 4; no carry, since shared
+  // memory addresses stay far below 2^18).
+  const uint64_t ad0 = ptx::smem_desc_k128_sw128(a0);
+  const uint64_t bd0 = ptx::smem_desc_k128_sw128(b0);
 #pragma unroll
   for (int k = 0; k < kBK / 32; ++k) {
-    const uint64_t ad = ptx::smem_desc_k128_sw128(a0 + 32 * k);
-    const uint64_t bd = ptx::smem_desc_k128_sw128(b0 + 32 * k);
+    const uint64_t ad = ad0 + 2u * k;
+    const uint64_t bd = bd0 + 2u * k;
     const uint32_t acc = (accumulate_first || k > 0) ? 1u : 0u;
     if (PAIR)
       ptx::mma_f8f6f4_pair(d, ad, bd, idesc, acc);
@@ -233,11 +249,16 @@ __device__ __forceinline__ void promote_step(float* acc, const uint32_t* v, floa
                                              const float* scb, int col0, float f_lo, float f_hi,
                                              int a_split) {
   if constexpr (B_TILE) {
-    // one broadcast 16-byte shared-memory read serves four columns
+    // one broadcast 16-byte shared-memory read serves four columns; the
+    // step's reads are all issued before its FMAs, so their latencies overlap
     const float2 sa2 = make_float2(sa_r, sa_r);
+    float4 sbv[kC / 4];
+#pragma unroll
+    for (int j = 0; j < kC; j += 4)
+      sbv[j / 4] = *reinterpret_cast<const float4*>(scb + col0 + a0 + j);
 #pragma unroll
     for (int j = 0; j < kC; j += 4) {
-      const float4 sb4 = *reinterpret_cast<const float4*>(scb + col0 + a0 + j);
+      const float4 sb4 = sbv[j / 4];
       const float2 p0 = make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
       const float2 p1 = make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
       const float2 r0 = ptx::fma2_rn(ptx::mul2_rn(p0, make_float2(sb4.x, sb4.y)), sa2,
@@ -432,21 +453,23 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
         if (PROMOTE) {
           for (int kb = 0; kb < KB; ++kb, ++it, ++kt) {
-            const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
-            if (!wait_bar<kMmaSuspend>(&tempty[buf], tph ^ 1, abort_flag, kErrMma)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
+            // The operands usually land long before the TMEM buffer comes
+            // back: wait for them first, so that once the promotion warps
+            // release the buffer only the MMAs remain to be issued.
             const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
             if (!wait_bar<kMmaSuspend>(&full[stage], phase, abort_flag, kErrMma)) {
               ok = false;
               break;
             }
-            ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
+            const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
             const uint32_t d = tmem_base + buf * L::kTmemStride;
+            if (!wait_bar<kMmaSuspend>(&tempty[buf], tph ^ 1, abort_flag, kErrMma)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
             issue_kgroup<PAIR>(d, a0, b0, kIdesc, false);
             commit_stage<PAIR>(&empty[stage]);
             if (PAIR)
@@ -553,37 +576,47 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         using PS = PromoSteps<kCols>;
         constexpr int kS = PS::kSteps;
         static_assert(kS <= 4, "steps");
+        // With double-buffered steps and an even step count, the first load
+        // of the next K-group goes into the buffer the last step does not
+        // use: it is issued right after this K-group's buffer is handed back,
+        // before the last step's FMAs, whenever the next partial is already
+        // there, so its latency overlaps those FMAs.
+        constexpr bool kPrefetch = !L::kLoadAll && !L::kSingleBuf && kS % 2 == 0;
         // Block scales: the first column of this warp's range that lies in
         // the next 128-column block (kCols when there is none).
         const int a_split = B_TILE ? kCols : ((n0 + col0) / 128 + 1) * 128 - (n0 + col0);
         const int nb_lo = (n0 + col0) / 128 - n0 / 128;
+        // this K-group's row scale and block factors, from its scale slot
+        auto read_scales = [&](const float* sc, float& sa_o, float& lo_o, float& hi_o) {
+          sa_o = sc[row];
+          lo_o = hi_o = 0.0f;
+          if (!B_TILE) {
+            lo_o = __fmul_rn(sa_o, sc[kBM + nb_lo]);
+            hi_o = a_split < kCols ? __fmul_rn(sa_o, sc[kBM + nb_lo + 1]) : lo_o;
+          }
+        };
+        uint32_t v[2][32];
+        bool pre = false;  // the first load of this K-group is already in v[0]
         for (int kb = 0; kb < KB; ++kb, ++kt, ++ks) {
           const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
           const uint32_t slot = ks % kScaleSlots, sph = (ks / kScaleSlots) & 1;
+          const float* sc = sScale + slot * L::kScaleFloats;
+          const float* scb = sc + kBM;
+          const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
+          float sa_r, f_lo, f_hi;
           bool w1 = wait_bar(&sfull[slot], sph, abort_flag, kErrPromo);
           if (!__all_sync(0xFFFFFFFFu, w1)) { ok = false; break; }
-          const float* sc = sScale + slot * L::kScaleFloats;
-          const float sa_r = sc[row];
-          const float* scb = sc + kBM;
-          float f_lo = 0.0f, f_hi = 0.0f;
-          if (!B_TILE) {
-            f_lo = __fmul_rn(sa_r, scb[nb_lo]);
-            f_hi = a_split < kCols ? __fmul_rn(sa_r, scb[nb_lo + 1]) : f_lo;
+          read_scales(sc, sa_r, f_lo, f_hi);
+          if (!pre) {
+            bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
+            if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
+            ptx::tc_fence_after();
           }
-          bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
-          if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
-          ptx::tc_fence_after();
-          // Software pipeline over the K-group's TMEM read steps: the load of
-          // step s+1 is issued right after step s's data has arrived and
-          // before step s's FMAs.  tcgen05.wait::ld waits for all of this
-          // thread's loads, which is why only one step is ever in flight.
-          const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
           if constexpr (L::kLoadAll) {
             // The whole partial of this warp in one round of loads; the
             // buffer goes back to the MMA issuer before the FMAs.
             uint32_t va[kCols];
-#pragma unroll
-            for (int c = 0; c < kCols; c += 16) ptx::tmem_ld_32x32b_x16(tcur + c, va + c);
+            ptx::tmem_ld_cols<kCols>(tcur, va);
             ptx::tmem_ld_wait();
             reg_fence<kCols>(va);
             ptx::tc_fence_before();
@@ -593,9 +626,35 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
             for (int c = 0; c < kCols; c += 16)
               promote_step<16, 0, B_TILE>(acc + c, va + c, sa_r, scb, col0 + c, f_lo, f_hi,
                                           a_split - c);
+          } else if constexpr (L::kSingleBuf) {
+            // One register buffer: load a step, wait, (after the last load)
+            // hand the buffer back, then the step's FMAs.
+            uint32_t* v1 = v[0];
+#define FP8BS_STEP1(S)                                                                    \
+  if constexpr (S < kS) {                                                                 \
+    tmem_ld_step<PS::width(S)>(tcur + 32 * (S), v1);                                      \
+    ptx::tmem_ld_wait();                                                                  \
+    reg_fence<PS::width(S)>(v1);                                                          \
+    if constexpr (S + 1 == kS) {                                                          \
+      ptx::tc_fence_before();                                                             \
+      __syncwarp();                                                                       \
+      if (lane == 0) release_tmem<PAIR>(&tempty[buf]);                                    \
+    }                                                                                     \
+    promote_step<PS::width(S), 32 * (S), B_TILE>(acc, v1, sa_r, scb, col0, f_lo, f_hi,    \
+                                                 a_split);                                \
+  }
+            FP8BS_STEP1(0)
+            FP8BS_STEP1(1)
+            FP8BS_STEP1(2)
+            FP8BS_STEP1(3)
+#undef FP8BS_STEP1
           } else {
-          uint32_t v[2][32];
-          tmem_ld_step<PS::width(0)>(tcur, v[0]);
+            // Double-buffered steps: the load of step s+1 is issued right
+            // after step s's data has arrived and before step s's FMAs
+            // (tcgen05.wait::ld waits for all of this thread's loads, so one
+            // step is in flight at a time).
+            if (!pre) tmem_ld_step<PS::width(0)>(tcur, v[0]);
+            pre = false;
 #define FP8BS_STEP(S)                                                                     \
   if constexpr (S < kS) {                                                                 \
     ptx::tmem_ld_wait();                                                                  \
@@ -607,14 +666,26 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       ptx::tc_fence_before();                                                             \
       __syncwarp();                                                                       \
       if (lane == 0) release_tmem<PAIR>(&tempty[buf]);                                    \
+      if constexpr (kPrefetch) {                                                          \
+        if (kb + 1 < KB) {                                                                \
+          const uint32_t nk = kt + 1, nbuf = nk % TBUF, ntph = (nk / TBUF) & 1;           \
+          if (__all_sync(0xFFFFFFFFu,                                                     \
+                         ptx::mbar_test_wait(ptx::smem_addr(&tfull[nbuf]), ntph))) {      \
+            ptx::tc_fence_after();                                                        \
+            tmem_ld_step<PS::width(0)>(tmem_base + t_lane + nbuf * L::kTmemStride + col0, \
+                                       v[0]);                                             \
+            pre = true;                                                                   \
+          }                                                                               \
+        }                                                                                 \
+      }                                                                                   \
     }                                                                                     \
     promote_step<PS::width(S), 32 * S, B_TILE>(acc, v[S & 1], sa_r, scb, col0, f_lo, f_hi, \
                                                a_split);                                  \
   }
-          FP8BS_STEP(0)
-          FP8BS_STEP(1)
-          FP8BS_STEP(2)
-          FP8BS_STEP(3)
+            FP8BS_STEP(0)
+            FP8BS_STEP(1)
+            FP8BS_STEP(2)
+            FP8BS_STEP(3)
 #undef FP8BS_STEP
           }
           __syncwarp();
@@ -874,6 +945,9 @@ enum TileShape {
   kTile256x224Pair = 5,
   kTile256x256Pair = 6,
   kTile256x192PairW12 = 7,
+  kTile256x256PairW16 = 8,
+  kTile256x192PairW16 = 9,
+  kTile256x128PairW16 = 10,
 };
 
 TileShape choose_tile(int64_t M, int64_t N, int sms) {
@@ -912,6 +986,12 @@ cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
     switch (shape) {
       case kTile256x192PairW12:
         return launch_variant<192, true, 12, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x256PairW16:
+        return launch_variant<256, true, 16, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x192PairW16:
+        return launch_variant<192, true, 16, PROMOTE, OUT, B_TILE>(g, stream);
+      case kTile256x128PairW16:
+        return launch_variant<128, true, 16, PROMOTE, OUT, B_TILE>(g, stream);
       case kTile256x128Pair:
         return launch_variant<128, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
       case kTile256x160Pair:

@@ -189,6 +189,7 @@ struct Q1 {
   static constexpr int kScratchBytes = 0;
   static constexpr uint32_t kTx = kStageBytes;
   static constexpr int kTeams = 1;
+  static constexpr bool kBulkStores = false;
   struct Params {
     uint8_t* q;
     float* s;
@@ -247,6 +248,7 @@ struct Q1E5 {
   static constexpr int kScratchBytes = 0;
   static constexpr uint32_t kTx = kStageBytes;
   static constexpr int kTeams = 1;
+  static constexpr bool kBulkStores = false;
   struct Params {
     uint8_t* e5;  // [M][3K/2]
     float* s5;    // [K/128][M]
@@ -331,6 +333,7 @@ struct Q2 {
   static constexpr int kScratchBytes = 128 * 128 + 2 * kTeamWarps * 4;
   static constexpr uint32_t kTx = kStageBytes;
   static constexpr int kTeams = 2;
+  static constexpr bool kBulkStores = false;
   struct Params {
     uint8_t* q;
     float* s;
@@ -421,14 +424,19 @@ struct Q2 {
 
 template <class Op>
 struct StreamSmem {
+  // Each team's scratch comes first, 1024-byte aligned (a bulk tensor store
+  // with the 128-byte swizzle reads its staging buffer from there), then the
+  // ring of input stages, then the barriers.
+  static constexpr int kScratchPerTeam = ((Op::kScratchBytes + 1023) / 1024) * 1024;
+  static constexpr int kOffScratch = 0;
+  static constexpr int kOffRing = Op::kTeams * kScratchPerTeam;
   static constexpr int kRing = Op::kStages * Op::kStageBytes;
-  static constexpr int kScratchPerTeam = ((Op::kScratchBytes + 127) / 128) * 128;
-  static constexpr int kOffScratch = kRing;
-  static constexpr int kOffBars = kOffScratch + Op::kTeams * kScratchPerTeam;
+  static constexpr int kOffBars = kOffRing + kRing;
   static constexpr int kBytes = kOffBars + 2 * Op::kStages * 8 + 16;
-  static constexpr int kAlloc = kBytes + 128;  // room to align the base to 128
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
   static_assert(Op::kStageBytes % 128 == 0, "stage alignment");
   static_assert(Op::kStages <= 32, "stage mask");
+  static_assert(kAlloc <= 232448, "shared memory");
   // team t consumes the tiles at ring positions t, t + kTeams, ..., so each
   // stage belongs to one team
   static_assert(Op::kStages % Op::kTeams == 0, "stages per team");
@@ -450,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint8_t* ring = smem;
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem + L::kOffRing;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
   uint64_t* empty = full + S;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + S);
@@ -520,15 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tm.empty = &empty[s];
       Op::consume(ring + s * Op::kStageBytes, tile, p, tm);
     }
+    // a team's bulk stores read its staging buffer and write the output:
+    // both are complete before the CTA exits
+    if constexpr (Op::kBulkStores) {
+      if (tm.tid == 0) ptx::bulk_wait_all();
+    }
   }
 }
 
-// ---------------------------------------------------------------------------
-// The two transposing quantizers are plain kernels, one 128 x 128 tile per
-// CTA: 16-byte loads into a shared-memory tile, every thread reading words
-// along rows (conflict-free) and writing its codes as 16- or 32-byte runs of
-// the transposed output.
-// ---------------------------------------------------------------------------
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
@@ -552,6 +559,7 @@ struct Q12 {
   static constexpr int kScratchBytes = Q2::kScratchBytes;
   static constexpr uint32_t kTx = kStageBytes;
   static constexpr int kTeams = 2;
+  static constexpr bool kBulkStores = false;
   static_assert(Q1::kStageBytes == kStageBytes && Q2::kStageBytes == kStageBytes, "tile size");
   static_assert(Q2::kTeams == kTeams && Q2::kTeamWarps == kConsumerWarps / kTeams, "teams");
   struct Params {
@@ -663,110 +671,186 @@ __global__ void tensor_scale_finalize_kernel(float* scale_word) {
   if (threadIdx.x == 0 && blockIdx.x == 0) *scale_word = group_scale(*scale_word);
 }
 
-// Q1T: 128x1 tiles (128 consecutive rows of one column), output transposed.
-// Thread (cp, part): column pair cp (0..63), rows 32 part .. 32 part + 31.
-// With DUAL the same shared-memory tile also yields the 1x128 tiles of its
-// rows (q, s, as Q1 writes them): grad_out quantized both ways from one
-// read.  grid = (K/128, M/128).
-template <bool DUAL>
-__global__ void __launch_bounds__(256) quant_act_128x1_kernel(
-    const uint16_t* __restrict__ x, int64_t M, int64_t K, uint8_t* __restrict__ qT,
-    float* __restrict__ sT, uint8_t* __restrict__ q, float* __restrict__ s) {
-  __shared__ uint4 tile[128 * 16];  // row r, 16-byte segment g at [r * 16 + g]
-  __shared__ uint32_t red[4][64];
-  const int t = threadIdx.x;
-  const int64_t k0 = (int64_t)blockIdx.x * kGroup;
-  const int64_t mb = blockIdx.y;
-  const int64_t m0 = mb * kGroup;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int idx = t + 256 * j;
-    tile[idx] = ld_stream_v4(x + (m0 + (idx >> 4)) * K + k0 + (idx & 15) * 8);
+// ---------------------------------------------------------------------------
+// The transposing quantizers (128x1 tiles written transposed) are ops of the
+// same streaming scheme.  A team of 8 warps turns one input tile into a
+// 128 x 128 tile of output codes (output rows = input columns, 128 tokens
+// each) and its 128 scales; it writes them into a staging buffer in its
+// shared-memory scratch, and one thread stores both with bulk copies (a 2-D
+// tensor store for the codes, a 512-byte copy for the scales).  The staging
+// layout is the tensor map's 128-byte swizzle: 16-byte chunk c of row k sits
+// at chunk c ^ (k % 8).  Each thread writes 16-byte chunks of several output
+// rows; the lanes pick the order of their rows so that every group of 8
+// lanes writes 8 different (k % 8) rows at once, which keeps the writes free
+// of bank conflicts.
+// ---------------------------------------------------------------------------
+
+// 16 bytes into row k, chunk c of a 128 x 128 staging tile (128-byte swizzle).
+__device__ __forceinline__ void stage_chunk(uint8_t* st, int k, int c, uint4 v) {
+  *reinterpret_cast<uint4*>(st + k * 128 + ((c ^ (k & 7)) << 4)) = v;
+}
+
+// The team's staging buffer is free again once the previous tile's bulk
+// stores (issued by the team's thread 0) have read it.
+__device__ __forceinline__ void team_stage_wait(const Team& tm) {
+  if (tm.tid == 0) ptx::bulk_wait_read_all();
+}
+
+// Store the staged tile: codes to (x = m0, y = k0) of the transposed output,
+// and 128 scales to sT_row.  Called by every team thread after its staging
+// writes.
+__device__ __forceinline__ void team_stage_store(const Team& tm, const CUtensorMap* map_out,
+                                                 const uint8_t* st, const float* st_scales,
+                                                 int m0, int k0, float* sT_row) {
+  ptx::fence_proxy_async_smem();
+  ptx::named_barrier(tm.bar, tm.threads);
+  if (tm.tid == 0) {
+    ptx::tma_store_2d(map_out, st, m0, k0);
+    ptx::bulk_store(sT_row, st_scales, 128 * 4);
+    ptx::bulk_commit();
   }
-  __syncthreads();
-  if constexpr (DUAL) {
-    // 1x128 tiles: half-warp h owns rows h, h + 16, ..., h + 112; lane l of
-    // it holds 8 consecutive elements of each, and lanes 0..7 compute the
-    // eight rows' scales.
+}
+
+// Q1T (and, with DUAL, Q1 of the same tile): 128x1 tiles of a bf16
+// activation (128 consecutive rows of one column), written transposed; with
+// DUAL also the 1x128 tiles of the same rows, as Q1 writes them (grad_out
+// quantized both ways from one read, page P2, paragraph 1).
+// Team thread (cp, part): column pair cp (0..63) and rows 32 part ..
+// 32 part + 31 of the 128 x 128 tile.
+template <bool DUAL>
+struct Q1TS {
+  static constexpr int kStageBytes = 128 * 256;
+  static constexpr int kStages = 4;
+  static constexpr int kTeams = 2;
+  static constexpr bool kBulkStores = true;
+  static constexpr int kOffScales = 128 * 128;
+  static constexpr int kOffRed = kOffScales + 128 * 4;
+  static constexpr int kScratchBytes = kOffRed + 2 * 4 * 64 * 4;
+  static constexpr uint32_t kTx = kStageBytes;
+  struct Params {
+    CUtensorMap map_out;  // qT [K][M] bytes, 128 x 128 box, 128-byte swizzle (64-byte aligned)
+    uint8_t* q;           // DUAL: [M][K]
+    float* s;             // DUAL: [K/128][M]
+    float* sT;            // [M/128][K]
+    int M, K, KB, num_tiles;
+  };
+  __device__ static void issue(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile,
+                               const Params& p) {
+    ptx::tma_load_2d(dst, map, bar, (tile % p.KB) * kGroup, (tile / p.KB) * kGroup);
+  }
+  __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
+                                 const Team& tm) {
+    const int kb = tile % p.KB, mb = tile / p.KB;
+    const int64_t k0 = (int64_t)kb * kGroup, m0 = (int64_t)mb * kGroup;
+    const int t = tm.tid;
+    const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage);
+    const int cp = t & 63, part = t >> 6;
     const int hw = t >> 4, l16 = t & 15;
-    uint4 v[8];
-    uint32_t mrow[8], prow[8];
-    bool nan_seen = false;
+    if constexpr (DUAL) {
+      // 1x128 tiles first (their registers are free again before the 128x1
+      // pass): half-warp hw owns rows hw, hw + 16, ..., hw + 112; lane l16
+      // holds 8 consecutive elements of each, lanes 0..7 compute the eight
+      // rows' scales.
+      uint4 v[8];
+      const uint4* st = reinterpret_cast<const uint4*>(stage);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[i] = tile[(hw + 16 * i) * 16 + l16];
-      uint32_t mm = halves_max(mag_pair_max(
-          mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y), v[i].z), v[i].w));
-#pragma unroll
-      for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
-      prow[i] = mrow[i] = mm;
-      nan_seen |= mm > kBf16Inf;
-    }
-    if (__any_sync(kFull, nan_seen)) {  // rare: recount without NaN
+      for (int i = 0; i < 8; ++i) v[i] = st[(hw + 16 * i) * 16 + l16];
+      uint32_t mrow[8], prow[8];
+      bool nan_seen = false;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        uint32_t mm = halves_max(mag_pair_max_no_nan(
-            mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
-                                v[i].z),
-            v[i].w));
+        uint32_t mm = halves_max(mag_pair_max(
+            mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y), v[i].z), v[i].w));
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
-        mrow[i] = mm;
+        prow[i] = mrow[i] = mm;
+        nan_seen |= mm > kBf16Inf;
+      }
+      if (__any_sync(kFull, nan_seen)) {  // rare: recount without NaN
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t mm = halves_max(mag_pair_max_no_nan(
+              mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
+                                  v[i].z),
+              v[i].w));
+#pragma unroll
+          for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
+          mrow[i] = mm;
+        }
+      }
+      uint32_t mj = 0, pj = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((l16 & 7) == i) {
+          mj = mrow[i];
+          pj = prow[i];
+        }
+      const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const GroupScale g = shfl_scale(mine, (tm.lane & 16) + i);
+        const int64_t r = m0 + hw + 16 * i;
+        *reinterpret_cast<uint2*>(p.q + r * p.K + k0 + l16 * 8) = codes_bf16x8(v[i], g);
+        if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
       }
     }
-    uint32_t mj = 0, pj = 0;
+    uint32_t w[32];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if ((l16 & 7) == i) {
-        mj = mrow[i];
-        pj = prow[i];
-      }
-    const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
+    for (int i = 0; i < 32; ++i) w[i] = tw[(part * 32 + i) * 64 + cp];
+    release_stage(tm.empty, tm.lane);
+    // 128x1 tiles: the column pair's maxima over this thread's 32 rows, the
+    // NaN-free maxima recounted only where a NaN was seen
+    uint32_t mp = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const GroupScale g = shfl_scale(mine, (t & 16) + i);
-      const int64_t r = m0 + hw + 16 * i;
-      *reinterpret_cast<uint2*>(q + r * K + k0 + l16 * 8) = codes_bf16x8(v[i], g);
-      if (l16 == i) s[(k0 / kGroup) * M + r] = mine.s;
+    for (int i = 0; i < 32; ++i) mp = mag_pair_max(mp, w[i]);
+    uint32_t mc = mp;
+    if (pair_has_nan(mp)) {
+      mc = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) mc = mag_pair_max_no_nan(mc, w[i]);
     }
-  }
-  const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
-  const int cp = t & 63, part = t >> 6;
-  uint32_t m = 0;
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) m = mag_pair_max(m, tw[(part * 32 + i) * 64 + cp]);
-  red[part][cp] = m;
-  __syncthreads();
-  uint32_t mp = 0;
+    uint8_t* scr = tm.scratch;
+    uint32_t* red = reinterpret_cast<uint32_t*>(scr + kOffRed);  // [2][4][64]
+    red[part * 64 + cp] = mp;
+    red[256 + part * 64 + cp] = mc;
+    team_stage_wait(tm);
+    ptx::named_barrier(tm.bar, tm.threads);
+    uint32_t mpa = 0, mca = 0;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) mp = __vmaxu2(mp, red[q][cp]);
-  uint32_t mn = mp;
-  if (pair_has_nan(mp)) {  // rare: recount this column pair without NaN
-    mn = 0;
-    for (int r = 0; r < 128; ++r) mn = mag_pair_max_no_nan(mn, tw[r * 64 + cp]);
-  }
-  const GroupScale glo = make_scale(mn & 0xFFFFu, (mp & 0xFFFFu) >= kBf16Inf, true);
-  const GroupScale ghi = make_scale(mn >> 16, (mp >> 16) >= kBf16Inf, true);
-  uint32_t olo[8], ohi[8];
+    for (int q = 0; q < 4; ++q) {
+      mpa = __vmaxu2(mpa, red[q * 64 + cp]);
+      mca = __vmaxu2(mca, red[256 + q * 64 + cp]);
+    }
+    const GroupScale glo = make_scale(mca & 0xFFFFu, (mpa & 0xFFFFu) >= kBf16Inf, true);
+    const GroupScale ghi = make_scale(mca >> 16, (mpa >> 16) >= kBf16Inf, true);
+    uint32_t olo[8], ohi[8];
 #pragma unroll
-  for (int i = 0; i < 32; i += 4) {
-    const uint32_t w0 = tw[(part * 32 + i) * 64 + cp];
-    const uint32_t w1 = tw[(part * 32 + i + 1) * 64 + cp];
-    const uint32_t w2 = tw[(part * 32 + i + 2) * 64 + cp];
-    const uint32_t w3 = tw[(part * 32 + i + 3) * 64 + cp];
-    // rows i .. i + 3 of each column
-    olo[i >> 2] = codes_bf16x4(__byte_perm(w0, w1, 0x5410), __byte_perm(w2, w3, 0x5410), glo);
-    ohi[i >> 2] = codes_bf16x4(__byte_perm(w0, w1, 0x7632), __byte_perm(w2, w3, 0x7632), ghi);
+    for (int i = 0; i < 32; i += 4) {
+      // rows i .. i + 3 of each column
+      olo[i >> 2] = codes_bf16x4(__byte_perm(w[i], w[i + 1], 0x5410),
+                                 __byte_perm(w[i + 2], w[i + 3], 0x5410), glo);
+      ohi[i >> 2] = codes_bf16x4(__byte_perm(w[i], w[i + 1], 0x7632),
+                                 __byte_perm(w[i + 2], w[i + 3], 0x7632), ghi);
+    }
+    // output rows 2 cp (lo) and 2 cp + 1 (hi), chunks 2 part and 2 part + 1;
+    // lanes with (cp / 4) odd write hi first
+    const bool hi_first = (cp >> 2) & 1;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const bool sel_hi = (c == 0) == hi_first;
+      const int k = 2 * cp + (sel_hi ? 1 : 0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 d = sel_hi ? make_uint4(ohi[4 * h], ohi[4 * h + 1], ohi[4 * h + 2], ohi[4 * h + 3])
+                               : make_uint4(olo[4 * h], olo[4 * h + 1], olo[4 * h + 2], olo[4 * h + 3]);
+        stage_chunk(scr, k, 2 * part + h, d);
+      }
+    }
+    float* sc = reinterpret_cast<float*>(scr + kOffScales);
+    if (part == 0) *reinterpret_cast<float2*>(sc + 2 * cp) = make_float2(glo.s, ghi.s);
+    team_stage_store(tm, &p.map_out, scr, sc, (int)m0, (int)k0, p.sT + (int64_t)mb * p.K + k0);
   }
-  uint4* dlo = reinterpret_cast<uint4*>(qT + (k0 + 2 * cp) * M + m0 + part * 32);
-  uint4* dhi = reinterpret_cast<uint4*>(qT + (k0 + 2 * cp + 1) * M + m0 + part * 32);
-  dlo[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-  dlo[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
-  dhi[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-  dhi[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
-  if (part == 0)
-    *reinterpret_cast<float2*>(sT + mb * K + k0 + 2 * cp) = make_float2(glo.s, ghi.s);
-}
+};
 
 // Four codes (one word) of one row, dequantized with that row's scale:
 // x_hat = decode(code) * s, one round-to-nearest multiply each.
@@ -780,13 +864,11 @@ __device__ __forceinline__ void dequant4(uint32_t w, float s, float (&o)[4]) {
   o[3] = b.y;
 }
 
-// Four E5M6 codes of one row (row r of a 128-column tile staged as its
-// 192-byte packed stream; columns 4 cq .. 4 cq + 3 are bytes 6 cq .. 6 cq + 5),
+// Four E5M6 codes (48 bits: lo word and the next 16 bits) of one row,
 // dequantized with that row's scale: one round-to-nearest multiply each.
-__device__ __forceinline__ void dequant4_e5m6(const uint16_t* t16, int r, int cq, float s,
+__device__ __forceinline__ void dequant4_e5m6(uint32_t lo, uint32_t hi16, float s,
                                               float (&o)[4]) {
-  const int h = r * 96 + 3 * cq;
-  const uint64_t w = (uint64_t)t16[h] | ((uint64_t)t16[h + 1] << 16) | ((uint64_t)t16[h + 2] << 32);
+  const uint64_t w = (uint64_t)lo | ((uint64_t)hi16 << 32);
   const float2 s2 = make_float2(s, s);
   const float2 a = ptx::mul2_rn(make_float2(e5m6_decode((uint32_t)w & 0xFFFu),
                                             e5m6_decode((uint32_t)(w >> 12) & 0xFFFu)), s2);
@@ -798,110 +880,134 @@ __device__ __forceinline__ void dequant4_e5m6(const uint16_t* t16, int r, int cq
   o[3] = b.y;
 }
 
-// Q3: 1x128 -> 128x1.  CTA tile = 128 rows (one 128-token group) x 128
-// columns (one K-group) of codes plus their 128 row scales.  Thread
-// (cq, part): columns 4 cq .. 4 cq + 3, rows 16 part .. 16 part + 15; the
-// values are dequantized once for the column maxima (float maxima that
-// propagate NaN; a column holding a NaN recounts without it) and again for
-// the codes.  grid = (K/128, M/128).
-// With E5 the input is the packed E5M6 cache ([M][3K/2] bytes, 1x128 scales
-// for a maximum of 65024) instead of E4M3 codes.
+// Q3: 1x128 -> 128x1 re-tiling of cached codes.  A stage holds a tile of
+// 128 rows (one 128-token group) x 128 columns (one K-group) of codes and
+// its 128 row scales (E4M3 codes, or with E5 the packed 12-bit E5M6 cache).
+// Team thread (cq, part): columns 4 cq .. 4 cq + 3, rows 16 part ..
+// 16 part + 15.  The column maxima propagate NaN (max.NaN) and, separately,
+// ignore it, so a column that holds a NaN needs no extra pass.
 template <bool E5>
-__global__ void __launch_bounds__(256) requant_1x128_to_128x1_kernel(
-    const uint8_t* __restrict__ q, const float* __restrict__ s, int64_t M, int64_t K,
-    uint8_t* __restrict__ qT, float* __restrict__ sT) {
-  constexpr int kSeg = E5 ? 12 : 8;  // 16-byte segments per tile row
-  __shared__ uint4 tile[128 * kSeg];  // row r, segment g at [r * kSeg + g]
-  __shared__ float srow[128];
-  __shared__ float red[8][128];
-  const int t = threadIdx.x;
-  const int64_t kb = blockIdx.x, mb = blockIdx.y;
-  const int64_t k0 = kb * kGroup, m0 = mb * kGroup;
-  const int64_t row_bytes = E5 ? K / 2 * 3 : K;
-  const int64_t col_byte = E5 ? kb * 192 : k0;
-#pragma unroll
-  for (int j = 0; j < kSeg / 2; ++j) {
-    const int idx = t + 256 * j;
-    tile[idx] = ld_stream_v4(q + (m0 + idx / kSeg) * row_bytes + col_byte + (idx % kSeg) * 16);
-  }
-  if (t < 128) srow[t] = s[kb * M + m0 + t];
-  __syncthreads();
-  const uint32_t* tw = reinterpret_cast<const uint32_t*>(tile);
-  const uint16_t* t16 = reinterpret_cast<const uint16_t*>(tile);
-  const int cq = t & 31, part = t >> 5;
-  auto dq = [&](int r, float (&xv)[4]) {
-    if constexpr (E5)
-      dequant4_e5m6(t16, r, cq, srow[r], xv);
-    else
-      dequant4(tw[r * 32 + cq], srow[r], xv);
+struct Q3S {
+  static constexpr int kRowBytes = E5 ? 192 : 128;
+  static constexpr int kCodeBytes = 128 * kRowBytes;
+  static constexpr int kStageBytes = kCodeBytes + 128 * 4;
+  static constexpr int kStages = E5 ? 4 : 6;
+  static constexpr int kTeams = 2;
+  static constexpr bool kBulkStores = true;
+  static constexpr int kOffScales = 128 * 128;
+  static constexpr int kOffRed = kOffScales + 128 * 4;
+  static constexpr int kScratchBytes = kOffRed + 2 * 8 * 128 * 4;
+  static constexpr uint32_t kTx = kStageBytes;
+  struct Params {
+    CUtensorMap map_out;  // qT [K][M] bytes, 128 x 128 box, 128-byte swizzle (64-byte aligned)
+    const float* s;       // [K/128][M]
+    float* sT;            // [M/128][K]
+    int M, K, KB, num_tiles;
   };
-  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  // The E5M6 decode is costly enough that the 16 x 4 values are decoded once
-  // and kept in registers for the code pass (96 registers, 2 CTAs per SM);
-  // for E4M3 the hardware conversions are cheap and occupancy wins (61
-  // registers, 4 CTAs per SM, decoding twice).
-  float xr[E5 ? 16 : 1][4];
-  if constexpr (E5) {
+  __device__ static void issue(const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile,
+                               const Params& p) {
+    const int kb = tile % p.KB, mb = tile / p.KB;
+    ptx::tma_load_2d(dst, map, bar, kb * kRowBytes, mb * kGroup);
+    ptx::bulk_load(dst + kCodeBytes, p.s + (int64_t)kb * p.M + (int64_t)mb * kGroup, 128 * 4,
+                   bar);
+  }
+  __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
+                                 const Team& tm) {
+    const int kb = tile % p.KB, mb = tile / p.KB;
+    const int64_t k0 = (int64_t)kb * kGroup, m0 = (int64_t)mb * kGroup;
+    const int t = tm.tid;
+    const int cq = t & 31, part = t >> 5;
+    const float* srow = reinterpret_cast<const float*>(stage + kCodeBytes) + part * 16;
+    // The raw codes and the row scales stay in registers (the stage goes
+    // back to the producer at once); each value is dequantized twice, for
+    // the column maxima and for the codes, which keeps the kernel within the
+    // registers that 17 warps per SM leave (96 per thread).
+    uint32_t w[16], wh[E5 ? 8 : 1];  // E5: 48 bits per row (w + 16 bits of wh)
+    float sr[16];
+    if constexpr (E5) {
+      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(stage);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      dq(part * 16 + i, xr[i]);
+      for (int i = 0; i < 16; ++i) {
+        const int h = (part * 16 + i) * 96 + 3 * cq;
+        w[i] = (uint32_t)t16[h] | ((uint32_t)t16[h + 1] << 16);
+        const uint32_t top = t16[h + 2];
+        if (i & 1)
+          wh[i >> 1] |= top << 16;
+        else
+          wh[i >> 1] = top;
+      }
+    } else {
+      const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xr[i][c]);
+      for (int i = 0; i < 16; ++i) w[i] = tw[(part * 16 + i) * 32 + cq];
     }
-  } else {
-#pragma unroll 4
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sr[i] = srow[i];
+    release_stage(tm.empty, tm.lane);
+    auto dq = [&](int i, float (&xv)[4]) {
+      if constexpr (E5)
+        dequant4_e5m6(w[i], (wh[i >> 1] >> (16 * (i & 1))) & 0xFFFFu, sr[i], xv);
+      else
+        dequant4(w[i], sr[i], xv);
+    };
+    float mn[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
       float xv[4];
-      dq(part * 16 + i, xv);
+      dq(i, xv);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) m[c] = fmax_abs_nan(m[c], xv[c]);
-    }
-  }
-  *reinterpret_cast<float4*>(&red[part][4 * cq]) = make_float4(m[0], m[1], m[2], m[3]);
-  __syncthreads();
-  GroupScale g[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float mp = 0.0f;  // NaN if the column holds a NaN
-#pragma unroll
-    for (int pp = 0; pp < 8; ++pp) mp = fmax_abs_nan(mp, red[pp][4 * cq + c]);
-    float mn = mp;
-    if (mp != mp) {  // rare: recount this column ignoring NaN
-      mn = 0.0f;
-      for (int r = 0; r < 128; ++r) {
-        float xv[4];
-        dq(r, xv);
-        mn = fmaxf(mn, fabsf(xv[c]));
+      for (int c = 0; c < 4; ++c) {
+        mn[c] = fmax_abs_nan(mn[c], xv[c]);
+        mc[c] = fmaxf(mc[c], fabsf(xv[c]));
       }
     }
-    g[c] = make_scale(__float_as_uint(mn), !(mp < __uint_as_float(kF32Inf)), false);
-  }
-  uint32_t o[4][4];
+    uint8_t* scr = tm.scratch;
+    float* red = reinterpret_cast<float*>(scr + kOffRed);  // [2][8][128]
+    *reinterpret_cast<float4*>(red + part * 128 + 4 * cq) = make_float4(mn[0], mn[1], mn[2], mn[3]);
+    *reinterpret_cast<float4*>(red + 1024 + part * 128 + 4 * cq) =
+        make_float4(mc[0], mc[1], mc[2], mc[3]);
+    team_stage_wait(tm);
+    ptx::named_barrier(tm.bar, tm.threads);
+    GroupScale g[4];
 #pragma unroll
-  for (int i = 0; i < 16; i += 4) {
-    if constexpr (E5) {
+    for (int c = 0; c < 4; ++c) {
+      float a = 0.0f, b = 0.0f;  // a is NaN if the column holds a NaN
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        o[c][i >> 2] = codes_f32x4(xr[i][c], xr[i + 1][c], xr[i + 2][c], xr[i + 3][c], g[c]);
-    } else {
-      const int r = part * 16 + i;
+      for (int q = 0; q < 8; ++q) {
+        a = fmax_abs_nan(a, red[q * 128 + 4 * cq + c]);
+        b = fmaxf(b, red[1024 + q * 128 + 4 * cq + c]);
+      }
+      g[c] = make_scale(__float_as_uint(b), !(a < __uint_as_float(kF32Inf)), false);
+    }
+    uint32_t o[4][4];
+#pragma unroll
+    for (int i = 0; i < 16; i += 4) {
       float x0[4], x1[4], x2[4], x3[4];
-      dq(r, x0);
-      dq(r + 1, x1);
-      dq(r + 2, x2);
-      dq(r + 3, x3);
+      dq(i, x0);
+      dq(i + 1, x1);
+      dq(i + 2, x2);
+      dq(i + 3, x3);
 #pragma unroll
       for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
     }
-  }
+    // output rows 4 cq + c', chunk = part; lane cq writes column
+    // c' = (c + cq / 2) % 4 at step c
+    const int rot = (cq >> 1) & 3;
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
-    *reinterpret_cast<uint4*>(qT + (k0 + 4 * cq + c) * M + m0 + part * 16) =
-        make_uint4(o[c][0], o[c][1], o[c][2], o[c][3]);
-  if (part == 0)
-    *reinterpret_cast<float4*>(sT + mb * K + k0 + 4 * cq) =
-        make_float4(g[0].s, g[1].s, g[2].s, g[3].s);
-}
+    for (int c = 0; c < 4; ++c) {
+      const int cc = (c + rot) & 3;
+      uint4 d = make_uint4(o[0][0], o[0][1], o[0][2], o[0][3]);
+      if (cc == 1) d = make_uint4(o[1][0], o[1][1], o[1][2], o[1][3]);
+      if (cc == 2) d = make_uint4(o[2][0], o[2][1], o[2][2], o[2][3]);
+      if (cc == 3) d = make_uint4(o[3][0], o[3][1], o[3][2], o[3][3]);
+      stage_chunk(scr, 4 * cq + cc, part, d);
+    }
+    float* sc = reinterpret_cast<float*>(scr + kOffScales);
+    if (part == 0)
+      *reinterpret_cast<float4*>(sc + 4 * cq) = make_float4(g[0].s, g[1].s, g[2].s, g[3].s);
+    team_stage_store(tm, &p.map_out, scr, sc, (int)m0, (int)k0, p.sT + (int64_t)mb * p.K + k0);
+  }
+};
 
 int num_sms_current_device() {
   int dev = 0, n = 0;
@@ -940,20 +1046,59 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, uint8_t*
   return launch_stream<Q1>(map, p, stream);
 }
 
+namespace {
+
+// Output tensor map of a transposing quantizer: qT [K][M] bytes, 128 x 128
+// boxes with the 128-byte swizzle of the staging buffers.
+bool make_out_map(CUtensorMap* map, uint8_t* qT, int64_t K, int64_t M) {
+  return make_tmap_2d(map, qT, 1, K, M, kGroup, kGroup, true);
+}
+
+template <bool DUAL>
+cudaError_t launch_q1t(const void* x, int64_t M, int64_t K, uint8_t* qT, float* sT, uint8_t* q,
+                       float* s, cudaStream_t stream) {
+  CUtensorMap map;
+  typename Q1TS<DUAL>::Params p;
+  if (!make_tmap_2d(&map, x, 2, M, K, kGroup, kGroup, false) || !make_out_map(&p.map_out, qT, K, M))
+    return cudaErrorInvalidValue;
+  p.q = q;
+  p.s = s;
+  p.sT = sT;
+  p.M = (int)M;
+  p.K = (int)K;
+  p.KB = (int)(K / kGroup);
+  p.num_tiles = (int)(M / kGroup) * p.KB;
+  return launch_stream<Q1TS<DUAL>>(map, p, stream);
+}
+
+template <bool E5>
+cudaError_t launch_q3(const uint8_t* q, const float* s, int64_t M, int64_t K, uint8_t* qT,
+                      float* sT, cudaStream_t stream) {
+  CUtensorMap map;
+  typename Q3S<E5>::Params p;
+  const int64_t row_bytes = E5 ? K / 2 * 3 : K;
+  if (!make_tmap_2d(&map, q, 1, M, row_bytes, Q3S<E5>::kRowBytes, kGroup, false) ||
+      !make_out_map(&p.map_out, qT, K, M))
+    return cudaErrorInvalidValue;
+  p.s = s;
+  p.sT = sT;
+  p.M = (int)M;
+  p.K = (int)K;
+  p.KB = (int)(K / kGroup);
+  p.num_tiles = (int)(M / kGroup) * p.KB;
+  return launch_stream<Q3S<E5>>(map, p, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, uint8_t* qT, float* sT,
                                    cudaStream_t stream) {
-  dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
-  quant_act_128x1_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
-                                                           qT, sT, nullptr, nullptr);
-  return cudaGetLastError();
+  return launch_q1t<false>(x, M, K, qT, sT, nullptr, nullptr, stream);
 }
 
 cudaError_t launch_quant_act_dual(const void* x, int64_t M, int64_t K, uint8_t* q, float* s,
                                   uint8_t* qT, float* sT, cudaStream_t stream) {
-  dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
-  quant_act_128x1_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x), M, K,
-                                                          qT, sT, q, s);
-  return cudaGetLastError();
+  return launch_q1t<true>(x, M, K, qT, sT, q, s, stream);
 }
 
 cudaError_t launch_quant_act_and_weight(const void* x, int64_t M, int64_t K, uint8_t* q,
@@ -1003,9 +1148,7 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uin
 
 cudaError_t launch_requant_1x128_to_128x1(const uint8_t* q, const float* s, int64_t M, int64_t K,
                                           uint8_t* qT, float* sT, cudaStream_t stream) {
-  dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
-  requant_1x128_to_128x1_kernel<false><<<grid, 256, 0, stream>>>(q, s, M, K, qT, sT);
-  return cudaGetLastError();
+  return launch_q3<false>(q, s, M, K, qT, sT, stream);
 }
 
 cudaError_t launch_quant_per_tensor(const void* x, int64_t n, uint8_t* q, float* scale,
@@ -1045,9 +1188,7 @@ cudaError_t launch_quant_act_e5m6(const void* x, int64_t M, int64_t K, uint8_t* 
 
 cudaError_t launch_requant_e5m6_to_128x1(const uint8_t* e5, const float* s5, int64_t M, int64_t K,
                                          uint8_t* qT, float* sT, cudaStream_t stream) {
-  dim3 grid((unsigned)(K / kGroup), (unsigned)(M / kGroup));
-  requant_1x128_to_128x1_kernel<true><<<grid, 256, 0, stream>>>(e5, s5, M, K, qT, sT);
-  return cudaGetLastError();
+  return launch_q3<true>(e5, s5, M, K, qT, sT, stream);
 }
 
 // The quantizers' error word, taken like the GEMM's (enqueue_take_gemm_error).

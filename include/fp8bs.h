@@ -195,8 +195,9 @@ fp8bs_status fp8bs_gemm_ex(const uint8_t *a, const float *sa,
  *                      compute one 256xBN tile together, each CTA loading
  *                      its own half of A and half of B (no copy is
  *                      multicast);
- *   ..._W12            the same with 12 promotion warps of 64 columns each
- *                      (8 otherwise).
+ *   ..._W12, ..._W16   the same with 12 or 16 promotion warps (8
+ *                      otherwise), which read the tensor-core partial sums
+ *                      out of tensor memory faster.
  */
 typedef enum {
   FP8BS_TILE_AUTO = -1,
@@ -207,7 +208,10 @@ typedef enum {
   FP8BS_TILE_256x192_PAIR = 4,
   FP8BS_TILE_256x224_PAIR = 5,
   FP8BS_TILE_256x256_PAIR = 6,
-  FP8BS_TILE_256x192_PAIR_W12 = 7
+  FP8BS_TILE_256x192_PAIR_W12 = 7,
+  FP8BS_TILE_256x256_PAIR_W16 = 8,
+  FP8BS_TILE_256x192_PAIR_W16 = 9,
+  FP8BS_TILE_256x128_PAIR_W16 = 10
 } fp8bs_tile_shape;
 
 /*

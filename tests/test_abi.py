@@ -148,24 +148,28 @@ def test_valid_call_without_gpu_reports_cuda_or_arch(libfp8bs):
 
 
 def test_maximum_sizes_rejected(libfp8bs):
-    """Sizes past what the kernels index (32-bit rows, 65535 grid rows) are
-    refused before anything is launched."""
+    """Sizes past what the kernels index (32-bit rows and tile counts, 65535
+    grid rows) are refused before anything is launched."""
     L, m = libfp8bs.lib(), libfp8bs
     big = 1 << 31
     assert L.fp8bs_quant_act_1x128(FAKE, big, 128, 0, FAKE, FAKE, None) == m.ERR_UNSUPPORTED_SHAPE
-    assert L.fp8bs_quant_act_1x128(FAKE, 128 * 65536, 128, 1, FAKE, FAKE, None) == \
+    assert L.fp8bs_quant_act_1x128(FAKE, 1 << 30, 128, 1, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_1x128(FAKE, 1 << 29, 1 << 20, 1, FAKE, FAKE, None) == \
         m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_quant_act_1x128(FAKE, 128, 128 * 65536, 0, FAKE, FAKE, None) == \
         m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_quant_weight_128x128(FAKE, 128 * 65536, 128, FAKE, FAKE, None, None, None) == \
         m.ERR_UNSUPPORTED_SHAPE
-    assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 128 * 65536, 128, FAKE, FAKE, None) == \
+    assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 1 << 30, 128, FAKE, FAKE, None) == \
         m.ERR_UNSUPPORTED_SHAPE
-    assert L.fp8bs_quant_act_dual(FAKE, 128 * 65536, 128, FAKE, FAKE, FAKE, FAKE, None) == \
+    assert L.fp8bs_requant_1x128_to_128x1(FAKE, FAKE, 128, 1 << 30, FAKE, FAKE, None) == \
+        m.ERR_UNSUPPORTED_SHAPE
+    assert L.fp8bs_quant_act_dual(FAKE, 1 << 30, 128, FAKE, FAKE, FAKE, FAKE, None) == \
         m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_quant_act_e5m6(FAKE, big, 128, FAKE, FAKE, None, None, None) == \
         m.ERR_UNSUPPORTED_SHAPE
-    assert L.fp8bs_requant_e5m6_to_128x1(FAKE, FAKE, 128 * 65536, 128, FAKE, FAKE, None) == \
+    assert L.fp8bs_requant_e5m6_to_128x1(FAKE, FAKE, 1 << 30, 128, FAKE, FAKE, None) == \
         m.ERR_UNSUPPORTED_SHAPE
     assert L.fp8bs_quant_act_and_weight(FAKE, big, 128, FAKE, FAKE, FAKE, 128, 128, FAKE, FAKE,
                                         None) == m.ERR_UNSUPPORTED_SHAPE

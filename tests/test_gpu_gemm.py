@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 BLOCK, TILE = 0, 1
 # every output-tile shape of the kernel (the automatic choice differs by shape)
-TILES = list(range(8))
+TILES = list(range(11))
 
 
 def _quantized_pair(oracle_mod, M, N, K, seed, bkind):
