@@ -65,7 +65,12 @@ namespace {
 constexpr int kBM = 128;
 constexpr int kBK = 128;            // one scale group per pipeline stage
 constexpr int kFirstPromoWarp = 4;  // warps 0..3 control, 4.. promotion
-constexpr int kScaleSlots = 8;
+// Scales reach the promotion warps through a ring of kScaleSlots slots of
+// kScaleGroup K-groups each: one barrier wait and one release per slot, not
+// per K-group.
+constexpr int kScaleGroup = 4;
+constexpr int kScaleSlots = 2;
+constexpr int kScaleEntries = kScaleGroup * kScaleSlots;
 constexpr int kSmemLimit = 232448;  // 227 KB: the opt-in maximum per block
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
@@ -103,6 +108,8 @@ template <bool SUSPEND = false>
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                          unsigned int site) {
   const uint32_t addr = ptx::smem_addr(bar);
+  // a phase that has already completed is seen by one non-blocking test
+  if (ptx::mbar_test_wait(addr, parity)) return true;
 #pragma unroll 1
   for (int i = 0; i < 256; ++i)
     if (try_wait<SUSPEND>(addr, parity)) return true;
@@ -164,14 +171,14 @@ struct Cfg {
   static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
   static constexpr int kScaleFloats = kBM + kScaleB;
   static constexpr int kNumBarsMax = 2 * 8 + 2 * 4 + 2 * kScaleSlots + 1;
-  static constexpr int kFixed = kScaleSlots * kScaleFloats * 4 + kNumBarsMax * 8 + 16 + 1024;
+  static constexpr int kFixed = kScaleEntries * kScaleFloats * 4 + kNumBarsMax * 8 + 16 + 1024;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / (kABytes + kBBytes);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static_assert(kStages >= 2, "shared memory");
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
   static constexpr int kOffScale = kOffB + kStages * kBBytes;
-  static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleFloats * 4;
+  static constexpr int kOffBar = kOffScale + kScaleEntries * kScaleFloats * 4;
   static constexpr int kNumBars = 2 * kStages + 2 * kTBuf + 2 * kScaleSlots + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kBytes = kOffMisc + 16;
@@ -513,21 +520,25 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   } else if (warp == 2) {
     // --------------------------------------------------------- scale loader
     if (PROMOTE) {
-      uint32_t ks = 0;
+      uint32_t se = 0, sph = 0;  // scale entry and its slot's phase
       bool ok = true;
       for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
         const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
         const int m0 = mt * kBM, n0 = nt * BN;
         const int nb_first = n0 / 128;
         const int nb_count = (n0 + BN - 1) / 128 - nb_first + 1;
-        for (int kb = 0; kb < KB; ++kb, ++ks) {
-          const uint32_t slot = ks % kScaleSlots, sph = (ks / kScaleSlots) & 1;
-          bool w = wait_bar(&sempty[slot], sph ^ 1, abort_flag, kErrScales);
-          if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+        const int kb_close = u + unit_stride >= p.num_units ? KB - 1 : KB;
+#pragma unroll 1
+        for (int kb = 0; kb < KB; ++kb) {
+          const uint32_t slot = se / kScaleGroup, sub = se % kScaleGroup;
+          if (sub == 0) {
+            bool w = wait_bar(&sempty[slot], sph ^ 1, abort_flag, kErrScales);
+            if (!__all_sync(0xFFFFFFFFu, w)) { ok = false; break; }
+          }
           // Asynchronous 4-byte copies (zero-filled outside the matrix) that
           // complete on sfull[slot]: the loader never waits for memory, so it
-          // runs up to kScaleSlots K-groups ahead of the promotion warps.
-          float* dst = sScale + slot * L::kScaleFloats;
+          // runs up to kScaleEntries K-groups ahead of the promotion warps.
+          float* dst = sScale + se * L::kScaleFloats;
 #pragma unroll
           for (int i = 0; i < kBM / 32; ++i) {
             const int r = lane + 32 * i, m = m0 + r;
@@ -547,7 +558,17 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
             const bool v = nb * 128 < p.N;
             ptx::cp_async_4(dstb + lane, v ? p.sb + (size_t)nb * KB + kb : p.sb, v);
           }
-          ptx::cp_async_arrive_noinc(&sfull[slot]);
+          // the slot is complete after its last K-group (or the CTA's last)
+          if (sub == kScaleGroup - 1 || kb == kb_close) {
+            ptx::cp_async_arrive_noinc(&sfull[slot]);
+            se = (slot + 1) * kScaleGroup;
+            if (se == kScaleEntries) {
+              se = 0;
+              sph ^= 1;
+            }
+          } else {
+            ++se;
+          }
         }
       }
       // no copy may still be in flight into shared memory when the CTA exits
@@ -563,7 +584,8 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     const int row = lg * 32 + lane;
     const int col0 = ch * kCols;
     const uint32_t t_lane = (uint32_t)(lg * 32) << 16;
-    uint32_t kt = 0, ks = 0;
+    uint32_t kt = 0;
+    uint32_t se = 0, sph = 0;  // scale entry (0 .. kScaleEntries-1) and its slot's phase
     bool ok = true;
     for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
       const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
@@ -576,15 +598,14 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         using PS = PromoSteps<kCols>;
         constexpr int kS = PS::kSteps;
         static_assert(kS <= 4, "steps");
-        // With double-buffered steps and an even step count, the first load
-        // of the next K-group goes into the buffer the last step does not
-        // use: it is issued right after this K-group's buffer is handed back,
-        // before the last step's FMAs, whenever the next partial is already
-        // there, so its latency overlaps those FMAs.
-        constexpr bool kPrefetch = !L::kLoadAll && !L::kSingleBuf && kS % 2 == 0;
         // Block scales: the first column of this warp's range that lies in
         // the next 128-column block (kCols when there is none).
-        const int a_split = B_TILE ? kCols : ((n0 + col0) / 128 + 1) * 128 - (n0 + col0);
+        // When the tile width and the warp's column range are whole 128-column
+        // blocks (the 256-wide pair with 8 promotion warps), the range lies
+        // in one block: one factor per K-group.
+        constexpr bool kOneBlock = B_TILE || (BN % 128 == 0 && kCols % 128 == 0);
+        const int a_split =
+            kOneBlock ? kCols : ((n0 + col0) / 128 + 1) * 128 - (n0 + col0);
         const int nb_lo = (n0 + col0) / 128 - n0 / 128;
         // this K-group's row scale and block factors, from its scale slot
         auto read_scales = [&](const float* sc, float& sa_o, float& lo_o, float& hi_o) {
@@ -592,26 +613,28 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
           lo_o = hi_o = 0.0f;
           if (!B_TILE) {
             lo_o = __fmul_rn(sa_o, sc[kBM + nb_lo]);
-            hi_o = a_split < kCols ? __fmul_rn(sa_o, sc[kBM + nb_lo + 1]) : lo_o;
+            hi_o = (!kOneBlock && a_split < kCols) ? __fmul_rn(sa_o, sc[kBM + nb_lo + 1]) : lo_o;
           }
         };
         uint32_t v[2][32];
-        bool pre = false;  // the first load of this K-group is already in v[0]
-        for (int kb = 0; kb < KB; ++kb, ++kt, ++ks) {
+        // the CTA's last K-group closes its scale slot early
+        const int kb_close = u + unit_stride >= p.num_units ? KB - 1 : KB;
+#pragma unroll 1
+        for (int kb = 0; kb < KB; ++kb, ++kt) {
           const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
-          const uint32_t slot = ks % kScaleSlots, sph = (ks / kScaleSlots) & 1;
-          const float* sc = sScale + slot * L::kScaleFloats;
+          const uint32_t slot = se / kScaleGroup, sub = se % kScaleGroup;
+          const float* sc = sScale + se * L::kScaleFloats;
           const float* scb = sc + kBM;
           const uint32_t tcur = tmem_base + t_lane + buf * L::kTmemStride + col0;
           float sa_r, f_lo, f_hi;
-          bool w1 = wait_bar(&sfull[slot], sph, abort_flag, kErrPromo);
-          if (!__all_sync(0xFFFFFFFFu, w1)) { ok = false; break; }
-          read_scales(sc, sa_r, f_lo, f_hi);
-          if (!pre) {
-            bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
-            if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
-            ptx::tc_fence_after();
+          if (sub == 0) {
+            bool w1 = wait_bar(&sfull[slot], sph, abort_flag, kErrPromo);
+            if (!__all_sync(0xFFFFFFFFu, w1)) { ok = false; break; }
           }
+          read_scales(sc, sa_r, f_lo, f_hi);
+          bool w2 = wait_bar(&tfull[buf], tph, abort_flag, kErrPromo);
+          if (!__all_sync(0xFFFFFFFFu, w2)) { ok = false; break; }
+          ptx::tc_fence_after();
           if constexpr (L::kLoadAll) {
             // The whole partial of this warp in one round of loads; the
             // buffer goes back to the MMA issuer before the FMAs.
@@ -653,8 +676,7 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
             // after step s's data has arrived and before step s's FMAs
             // (tcgen05.wait::ld waits for all of this thread's loads, so one
             // step is in flight at a time).
-            if (!pre) tmem_ld_step<PS::width(0)>(tcur, v[0]);
-            pre = false;
+            tmem_ld_step<PS::width(0)>(tcur, v[0]);
 #define FP8BS_STEP(S)                                                                     \
   if constexpr (S < kS) {                                                                 \
     ptx::tmem_ld_wait();                                                                  \
@@ -666,18 +688,6 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       ptx::tc_fence_before();                                                             \
       __syncwarp();                                                                       \
       if (lane == 0) release_tmem<PAIR>(&tempty[buf]);                                    \
-      if constexpr (kPrefetch) {                                                          \
-        if (kb + 1 < KB) {                                                                \
-          const uint32_t nk = kt + 1, nbuf = nk % TBUF, ntph = (nk / TBUF) & 1;           \
-          if (__all_sync(0xFFFFFFFFu,                                                     \
-                         ptx::mbar_test_wait(ptx::smem_addr(&tfull[nbuf]), ntph))) {      \
-            ptx::tc_fence_after();                                                        \
-            tmem_ld_step<PS::width(0)>(tmem_base + t_lane + nbuf * L::kTmemStride + col0, \
-                                       v[0]);                                             \
-            pre = true;                                                                   \
-          }                                                                               \
-        }                                                                                 \
-      }                                                                                   \
     }                                                                                     \
     promote_step<PS::width(S), 32 * S, B_TILE>(acc, v[S & 1], sa_r, scb, col0, f_lo, f_hi, \
                                                a_split);                                  \
@@ -688,8 +698,18 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
             FP8BS_STEP(3)
 #undef FP8BS_STEP
           }
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&sempty[slot]);
+          if (sub == kScaleGroup - 1 || kb == kb_close) {
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sempty[slot]);
+            // the next K-group starts the next slot
+            se = (slot + 1) * kScaleGroup;
+            if (se == kScaleEntries) {
+              se = 0;
+              sph ^= 1;
+            }
+          } else {
+            ++se;
+          }
         }
         if (!ok) break;
       } else {

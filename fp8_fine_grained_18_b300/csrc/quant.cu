@@ -755,7 +755,8 @@ struct Q1TS {
       const uint4* st = reinterpret_cast<const uint4*>(stage);
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = st[(hw + 16 * i) * 16 + l16];
-      uint32_t mrow[8], prow[8];
+      // lane j (of 0..7) of the half-warp keeps row j's maxima
+      uint32_t mj = 0, pj = 0;
       bool nan_seen = false;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -763,7 +764,7 @@ struct Q1TS {
             mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y), v[i].z), v[i].w));
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
-        prow[i] = mrow[i] = mm;
+        if ((l16 & 7) == i) pj = mj = mm;
         nan_seen |= mm > kBf16Inf;
       }
       if (__any_sync(kFull, nan_seen)) {  // rare: recount without NaN
@@ -775,16 +776,9 @@ struct Q1TS {
               v[i].w));
 #pragma unroll
           for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
-          mrow[i] = mm;
+          if ((l16 & 7) == i) mj = mm;
         }
       }
-      uint32_t mj = 0, pj = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if ((l16 & 7) == i) {
-          mj = mrow[i];
-          pj = prow[i];
-        }
       const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -918,50 +912,33 @@ struct Q3S {
     const int t = tm.tid;
     const int cq = t & 31, part = t >> 5;
     const float* srow = reinterpret_cast<const float*>(stage + kCodeBytes) + part * 16;
-    // The raw codes and the row scales stay in registers (the stage goes
-    // back to the producer at once); each value is dequantized twice, for
-    // the column maxima and for the codes, which keeps the kernel within the
-    // registers that 17 warps per SM leave (96 per thread).
-    uint32_t w[16], wh[E5 ? 8 : 1];  // E5: 48 bits per row (w + 16 bits of wh)
-    float sr[16];
-    if constexpr (E5) {
-      const uint16_t* t16 = reinterpret_cast<const uint16_t*>(stage);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int h = (part * 16 + i) * 96 + 3 * cq;
-        w[i] = (uint32_t)t16[h] | ((uint32_t)t16[h + 1] << 16);
-        const uint32_t top = t16[h + 2];
-        if (i & 1)
-          wh[i >> 1] |= top << 16;
-        else
-          wh[i >> 1] = top;
+    // Each value is dequantized twice, for the column maxima and for the
+    // codes, straight from the stage (which goes back to the producer after
+    // the second pass): this keeps the kernel within the registers that 17
+    // warps per SM leave (96 per thread).
+    uint8_t* scr = tm.scratch;
+    const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage);
+    const uint16_t* t16 = reinterpret_cast<const uint16_t*>(stage);
+    auto dq = [&](int i, float s_row, float (&xv)[4]) {
+      const int r = part * 16 + i;
+      if constexpr (E5) {
+        const int h = r * 96 + 3 * cq;
+        dequant4_e5m6((uint32_t)t16[h] | ((uint32_t)t16[h + 1] << 16), t16[h + 2], s_row, xv);
+      } else {
+        dequant4(tw[r * 32 + cq], s_row, xv);
       }
-    } else {
-      const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = tw[(part * 16 + i) * 32 + cq];
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) sr[i] = srow[i];
-    release_stage(tm.empty, tm.lane);
-    auto dq = [&](int i, float (&xv)[4]) {
-      if constexpr (E5)
-        dequant4_e5m6(w[i], (wh[i >> 1] >> (16 * (i & 1))) & 0xFFFFu, sr[i], xv);
-      else
-        dequant4(w[i], sr[i], xv);
     };
     float mn[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
+#pragma unroll 4
     for (int i = 0; i < 16; ++i) {
       float xv[4];
-      dq(i, xv);
+      dq(i, srow[i], xv);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         mn[c] = fmax_abs_nan(mn[c], xv[c]);
         mc[c] = fmaxf(mc[c], fabsf(xv[c]));
       }
     }
-    uint8_t* scr = tm.scratch;
     float* red = reinterpret_cast<float*>(scr + kOffRed);  // [2][8][128]
     *reinterpret_cast<float4*>(red + part * 128 + 4 * cq) = make_float4(mn[0], mn[1], mn[2], mn[3]);
     *reinterpret_cast<float4*>(red + 1024 + part * 128 + 4 * cq) =
@@ -982,14 +959,16 @@ struct Q3S {
     uint32_t o[4][4];
 #pragma unroll
     for (int i = 0; i < 16; i += 4) {
+      const float4 s4 = *reinterpret_cast<const float4*>(srow + i);
       float x0[4], x1[4], x2[4], x3[4];
-      dq(i, x0);
-      dq(i + 1, x1);
-      dq(i + 2, x2);
-      dq(i + 3, x3);
+      dq(i, s4.x, x0);
+      dq(i + 1, s4.y, x1);
+      dq(i + 2, s4.z, x2);
+      dq(i + 3, s4.w, x3);
 #pragma unroll
       for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
     }
+    release_stage(tm.empty, tm.lane);
     // output rows 4 cq + c', chunk = part; lane cq writes column
     // c' = (c + cq / 2) % 4 at step c
     const int rot = (cq >> 1) & 3;
