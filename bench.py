@@ -259,7 +259,13 @@ def run_ours(args):
 
     w = synth.WORKLOADS[WORKLOAD]
     M, N, K = w.M, w.N, w.K
-    inp = synth.make_inputs(WORKLOAD, seed=rank_seed(w.seed, rank))
+    if args.shape:
+        # another size with the same input recipe (for smaller profiler captures)
+        M, N, K = (int(x) for x in args.shape.split(","))
+        rng = np.random.default_rng(rank_seed(w.seed, rank))
+        inp = {"A": synth.loguniform_rows(rng, (M, K)), "B": synth.loguniform_rows(rng, (N, K))}
+    else:
+        inp = synth.make_inputs(WORKLOAD, seed=rank_seed(w.seed, rank))
     a_host = torch.from_numpy(inp["A"].view(np.int16)).view(torch.bfloat16)
     b_host = torch.from_numpy(inp["B"].view(np.int16)).view(torch.bfloat16)
     a = a_host.to(dev)
@@ -345,10 +351,13 @@ def run_ours(args):
 
     # End to end through the C ABI from pinned host buffers: every step
     # copies both operands host->device, runs the path and reads C back.
-    e2e = measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, max(3, min(args.steps, 10)))
-    e2e_ms = max_over_ranks(e2e.pop("_ms"), dist, dev)
-    e2e["value"] = round(whole_job_rate(flops, world, 1, e2e_ms) / 1e12, 2)
-    e2e["ms_per_step"] = round(e2e_ms, 3)
+    e2e = None
+    if args.e2e:
+        e2e = measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K,
+                          max(3, min(args.steps, 10)))
+        e2e_ms = max_over_ranks(e2e.pop("_ms"), dist, dev)
+        e2e["value"] = round(whole_job_rate(flops, world, 1, e2e_ms) / 1e12, 2)
+        e2e["ms_per_step"] = round(e2e_ms, 3)
 
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -371,7 +380,7 @@ def run_ours(args):
     # the per-row details are a single-GPU measurement: under torchrun they
     # would hold every GPU while rank 0 alone runs them
     if args.rows and world == 1:
-        out["rows"] = measure_rows(fp8bs, torch, dev, peaks, local_rank)
+        out["rows"] = measure_rows(fp8bs, torch, dev, peaks, local_rank, args.rows_only)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(M, N, K, inp, budget_s=20.0)
     if world > 1:
@@ -490,10 +499,11 @@ def _clock_brief(sampler):
     return {"sm_mhz": sm["sm_mhz"], "samples": sm["samples"], "reasons": sm["reasons"]}
 
 
-def measure_rows(fp8bs, torch, dev, peaks, index):
+def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
     """Every hot-path row at its own workload, and every quantizer at the
     8192 x 16384 bandwidth shape: quantizer GB/s, GEMM TFLOP/s; each row with
-    the SM clock sampled while it ran."""
+    the SM clock sampled while it ran.  With `only`, just the rows whose name
+    contains it are timed (their inputs are still prepared)."""
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
@@ -504,7 +514,12 @@ def measure_rows(fp8bs, torch, dev, peaks, index):
             ms, n = _time_ms(fn, torch, flush)
         return ms, n, _clock_brief(smp)
 
+    def skip(name):
+        return only is not None and only not in name
+
     def gemm_row(name, qa, sa, qb, sb, bkind, out_dtype, promote=True):
+        if skip(name):
+            return
         M, K = qa.shape
         N = qb.shape[0]
         c = torch.empty((M, N), dtype=out_dtype, device=dev)
@@ -515,6 +530,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index):
                       "frac_fp8_peak": round(tf / fp8_peak, 4), "launches": n, "clocks": clk}
 
     def quant_row(name, fn, nbytes):
+        if skip(name):
+            return
         ms, n, clk = timed(fn)
         gbs = nbytes / (ms * 1e-3) / 1e9
         rows[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
@@ -528,6 +545,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index):
     # torch._scaled_mm, one scale per tensor, no fine-grained scales and no
     # CUDA-core promotion), 8192^3, bf16 out.
     try:
+        if skip("context: library FP8 GEMM"):
+            raise LookupError("not selected")
         n = 8192
         x8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
         y8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
@@ -538,6 +557,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index):
             "ms": round(ms, 4), "TFLOP/s": round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1),
             "clocks": clk}
         del x8, y8
+    except LookupError:
+        pass
     except Exception as e:  # noqa: BLE001 -- context only
         rows["context: library FP8 GEMM (per-tensor scales) 8192^3 bf16"] = {"error": str(e)[:120]}
 
@@ -552,10 +573,11 @@ def measure_rows(fp8bs, torch, dev, peaks, index):
     def dense_step():
         fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb)
         fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=cd)
-    ms, n, clk = timed(dense_step)
-    tf = 2.0 * 4096 * 7168 * 7168 / (ms * 1e-3) / 1e12
-    rows["dense step 4096x7168x7168: Q1 of A + Q2 of W (one launch), G1 bf16"] = {
-        "ms": round(ms, 4), "TFLOP/s": round(tf, 1), "launches": n, "clocks": clk}
+    name = "dense step 4096x7168x7168: Q1 of A + Q2 of W (one launch), G1 bf16"
+    if not skip(name):
+        ms, n, clk = timed(dense_step)
+        tf = 2.0 * 4096 * 7168 * 7168 / (ms * 1e-3) / 1e12
+        rows[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "launches": n, "clocks": clk}
     quant_row("Q1+Q2 dense A 4096x7168 + W 7168x7168 (one launch)",
               lambda: fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb),
               algorithmic_bytes_q1(4096, 7168) + algorithmic_bytes_q2(7168, 7168))
@@ -577,21 +599,24 @@ def measure_rows(fp8bs, torch, dev, peaks, index):
     gemm_row("G1 moe 8192x4096x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
     # the GEMM output quantized for the next layer: fused epilogue against
     # the BF16 output written to HBM and quantized by Q1 afterwards
-    c8, cs8 = fp8bs.gemm_quant_out(qa, sa, qb, sb, 0)
-    ms_f, n, clk = timed(lambda: fp8bs.gemm_quant_out(qa, sa, qb, sb, 0, out=c8, out_scales=cs8))
-    cbf = torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev)
-    qc, sc = fp8bs.quant_act_1x128(cbf)
+    name = "G1+Q moe 8192x4096x7168, output quantized 1x128 in the epilogue"
+    if not skip(name):
+        c8, cs8 = fp8bs.gemm_quant_out(qa, sa, qb, sb, 0)
+        ms_f, n, clk = timed(lambda: fp8bs.gemm_quant_out(qa, sa, qb, sb, 0, out=c8, out_scales=cs8))
+        cbf = torch.empty((8192, 4096), dtype=torch.bfloat16, device=dev)
+        qc, sc = fp8bs.quant_act_1x128(cbf)
 
-    def unfused():
-        fp8bs.gemm(qa, sa, qb, sb, 0, out_dtype=torch.bfloat16, out=cbf)
-        fp8bs.quant_act_1x128(cbf, q=qc, scales=sc)
-    ms_u, _, _ = timed(unfused)
-    tflop = 2.0 * 8192 * 4096 * 7168 / 1e12
-    rows["G1+Q moe 8192x4096x7168, output quantized 1x128 in the epilogue"] = {
-        "ms": round(ms_f, 4), "TFLOP/s": round(tflop / (ms_f * 1e-3), 1),
-        "frac_fp8_peak": round(tflop / (ms_f * 1e-3) / fp8_peak, 4),
-        "unfused_gemm_bf16_then_Q1_ms": round(ms_u, 4), "launches": n, "clocks": clk}
-    del a, b, qa, sa, qb, sb, c8, cs8, cbf, qc, sc
+        def unfused():
+            fp8bs.gemm(qa, sa, qb, sb, 0, out_dtype=torch.bfloat16, out=cbf)
+            fp8bs.quant_act_1x128(cbf, q=qc, scales=sc)
+        ms_u, _, _ = timed(unfused)
+        tflop = 2.0 * 8192 * 4096 * 7168 / 1e12
+        rows[name] = {
+            "ms": round(ms_f, 4), "TFLOP/s": round(tflop / (ms_f * 1e-3), 1),
+            "frac_fp8_peak": round(tflop / (ms_f * 1e-3) / fp8_peak, 4),
+            "unfused_gemm_bf16_then_Q1_ms": round(ms_u, 4), "launches": n, "clocks": clk}
+        del c8, cs8, cbf, qc, sc
+    del a, b, qa, sa, qb, sb
 
     # backward chain at its own shapes
     bwd = synth.make_inputs("bwd")
@@ -755,6 +780,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rows", type=int, default=1, help="also time every hot-path row (1/0)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e", type=int, default=1, help="also measure end to end from host (1/0)")
+    ap.add_argument("--shape", default=None,
+                    help="M,N,K of the step in place of the workload's (profiling)")
+    ap.add_argument("--rows-only", default=None, help="time only the rows containing this text")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

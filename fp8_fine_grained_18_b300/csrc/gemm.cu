@@ -251,21 +251,25 @@ struct PromoSteps {
 // column a0 of the warp's kCols (tile column col0 + a0).  Block scales
 // change only at 128-column boundaries, which fall on multiples of 16
 // columns of the warp's range; tile scales change per column.
-template <int kC, int a0, bool B_TILE>
+template <int kC, int a0, bool B_TILE, int kBatch = 32>
 __device__ __forceinline__ void promote_step(float* acc, const uint32_t* v, float sa_r,
                                              const float* scb, int col0, float f_lo, float f_hi,
                                              int a_split) {
   if constexpr (B_TILE) {
     // one broadcast 16-byte shared-memory read serves four columns; the
-    // step's reads are all issued before its FMAs, so their latencies overlap
+    // reads of a batch of kBatch columns are all issued before its FMAs, so
+    // their latencies overlap
     const float2 sa2 = make_float2(sa_r, sa_r);
-    float4 sbv[kC / 4];
-#pragma unroll
-    for (int j = 0; j < kC; j += 4)
-      sbv[j / 4] = *reinterpret_cast<const float4*>(scb + col0 + a0 + j);
+    constexpr int kB = kBatch < kC ? kBatch : kC;
+    float4 sbv[kB / 4];
 #pragma unroll
     for (int j = 0; j < kC; j += 4) {
-      const float4 sb4 = sbv[j / 4];
+      if (j % kB == 0) {
+#pragma unroll
+        for (int i = 0; i < kB; i += 4)
+          sbv[i / 4] = *reinterpret_cast<const float4*>(scb + col0 + a0 + j + i);
+      }
+      const float4 sb4 = sbv[(j % kB) / 4];
       const float2 p0 = make_float2(__uint_as_float(v[j]), __uint_as_float(v[j + 1]));
       const float2 p1 = make_float2(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
       const float2 r0 = ptx::fma2_rn(ptx::mul2_rn(p0, make_float2(sb4.x, sb4.y)), sa2,
@@ -663,8 +667,8 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       __syncwarp();                                                                       \
       if (lane == 0) release_tmem<PAIR>(&tempty[buf]);                                    \
     }                                                                                     \
-    promote_step<PS::width(S), 32 * (S), B_TILE>(acc, v1, sa_r, scb, col0, f_lo, f_hi,    \
-                                                 a_split);                                \
+    promote_step<PS::width(S), 32 * (S), B_TILE, 16>(acc, v1, sa_r, scb, col0, f_lo, f_hi, \
+                                                     a_split);                            \
   }
             FP8BS_STEP1(0)
             FP8BS_STEP1(1)

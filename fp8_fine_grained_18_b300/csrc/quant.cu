@@ -131,6 +131,32 @@ struct Team {
   uint64_t* empty;   // empty barrier of the stage being consumed
 };
 
+// 16 bytes into row k, chunk c of a 128 x 128 staging tile (128-byte swizzle).
+__device__ __forceinline__ void stage_chunk(uint8_t* st, int k, int c, uint4 v) {
+  *reinterpret_cast<uint4*>(st + k * 128 + ((c ^ (k & 7)) << 4)) = v;
+}
+
+// The team's staging buffer is free again once the previous tile's bulk
+// stores (issued by the team's thread 0) have read it.
+__device__ __forceinline__ void team_stage_wait(const Team& tm) {
+  if (tm.tid == 0) ptx::bulk_wait_read_all();
+}
+
+// Store the staged tile: codes to (x = m0, y = k0) of the transposed output,
+// and 128 scales to sT_row.  Called by every team thread after its staging
+// writes.
+__device__ __forceinline__ void team_stage_store(const Team& tm, const CUtensorMap* map_out,
+                                                 const uint8_t* st, const float* st_scales,
+                                                 int m0, int k0, float* sT_row) {
+  ptx::fence_proxy_async_smem();
+  ptx::named_barrier(tm.bar, tm.threads);
+  if (tm.tid == 0) {
+    ptx::tma_store_2d(map_out, st, m0, k0);
+    ptx::bulk_store(sT_row, st_scales, 128 * 4);
+    ptx::bulk_commit();
+  }
+}
+
 // Q1's per-row maxima: half-warp rows h, h+32, h+64, h+96, eight bf16 of
 // each per lane (v[i] for row i).  Returns in lane j (0..3) of the half-warp
 // row j's NaN-free max magnitude (mj) and its plain max (pj >= Inf flags a
@@ -330,14 +356,19 @@ struct Q2 {
   static constexpr int kStageBytes = 128 * 256;
   static constexpr int kStages = 4;
   static constexpr int kTeamWarps = 8;
-  static constexpr int kScratchBytes = 128 * 128 + 2 * kTeamWarps * 4;
+  // scratch: the transposed copy's staging tile (1024-byte aligned, first),
+  // the block's code tile, the max reduction
+  static constexpr int kOffCodes = 128 * 128;
+  static constexpr int kOffRed = kOffCodes + 128 * 128;
+  static constexpr int kScratchBytes = kOffRed + 2 * kTeamWarps * 4;
   static constexpr uint32_t kTx = kStageBytes;
   static constexpr int kTeams = 2;
-  static constexpr bool kBulkStores = false;
+  static constexpr bool kBulkStores = true;
   struct Params {
+    CUtensorMap map_t;  // qT [K][N] bytes, 128 x 128 box, 128-byte swizzle (64-byte aligned)
     uint8_t* q;
     float* s;
-    uint8_t* qT;
+    uint8_t* qT;  // null: no transposed copy
     float* sT;
     int N, K, KB, NB, num_tiles;
   };
@@ -350,8 +381,8 @@ struct Q2 {
     const int kb = tile % p.KB, nb = tile / p.KB;
     const int t = tm.tid;
     const uint4* st = reinterpret_cast<const uint4*>(stage);
-    uint2* ctile = reinterpret_cast<uint2*>(tm.scratch);
-    uint32_t* red = reinterpret_cast<uint32_t*>(tm.scratch + 128 * 128);
+    uint2* ctile = reinterpret_cast<uint2*>(tm.scratch + kOffCodes);
+    uint32_t* red = reinterpret_cast<uint32_t*>(tm.scratch + kOffRed);
     uint4 v[8];
     uint32_t m2 = 0;
 #pragma unroll
@@ -361,6 +392,7 @@ struct Q2 {
                         v[j].w);
     }
     release_stage(tm.empty, tm.lane);
+    if (p.qT) team_stage_wait(tm);  // the staging tile is free again
     uint32_t m = halves_max(m2);
     const bool nan_here = m > kBf16Inf;
 #pragma unroll
@@ -402,21 +434,43 @@ struct Q2 {
       if (p.sT) p.sT[(int64_t)kb * p.NB + nb] = g.s;
     }
     if (p.qT) {
+      // The transposed copy: thread (kq, chunk) reads words kq (codes
+      // 4 kq .. 4 kq + 3) of rows 16 chunk .. 16 chunk + 15 of the code tile,
+      // transposes the 16 x 4 bytes with byte permutes into output rows
+      // 4 kq + c (16 codes each), and stages them for one tensor store.
       ptx::named_barrier(tm.bar, tm.threads);
-      const uint8_t* cb = reinterpret_cast<const uint8_t*>(ctile);
-      const int k = t & 127, h = t >> 7;  // output row k, rows h*64 .. h*64+63 of the block
+      const uint32_t* cw = reinterpret_cast<const uint32_t*>(ctile);
+      const int kq = t & 31, chunk = t >> 5;
+      uint32_t w[16];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t o[8];
+      for (int i = 0; i < 16; ++i) w[i] = cw[(16 * chunk + i) * 32 + kq];
+      uint32_t o[4][4];  // o[c][j]: output row 4 kq + c, rows 4 j .. 4 j + 3 of the chunk
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int n = h * 64 + half * 32 + 4 * i;
-          o[i] = (uint32_t)cb[n * 128 + k] | ((uint32_t)cb[(n + 1) * 128 + k] << 8) |
-                 ((uint32_t)cb[(n + 2) * 128 + k] << 16) | ((uint32_t)cb[(n + 3) * 128 + k] << 24);
-        }
-        uint4* d = reinterpret_cast<uint4*>(p.qT + (k0 + k) * p.N + n0 + h * 64 + half * 32);
-        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t a = w[4 * j], b = w[4 * j + 1], c = w[4 * j + 2], d = w[4 * j + 3];
+        const uint32_t ab01 = __byte_perm(a, b, 0x5140), cd01 = __byte_perm(c, d, 0x5140);
+        const uint32_t ab23 = __byte_perm(a, b, 0x7362), cd23 = __byte_perm(c, d, 0x7362);
+        o[0][j] = __byte_perm(ab01, cd01, 0x5410);
+        o[1][j] = __byte_perm(ab01, cd01, 0x7632);
+        o[2][j] = __byte_perm(ab23, cd23, 0x5410);
+        o[3][j] = __byte_perm(ab23, cd23, 0x7632);
+      }
+      // lane kq writes row c' = (c + kq / 2) % 4 at step c (conflict-free)
+      const int rot = (kq >> 1) & 3;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int cc = (c + rot) & 3;
+        uint4 d = make_uint4(o[0][0], o[0][1], o[0][2], o[0][3]);
+        if (cc == 1) d = make_uint4(o[1][0], o[1][1], o[1][2], o[1][3]);
+        if (cc == 2) d = make_uint4(o[2][0], o[2][1], o[2][2], o[2][3]);
+        if (cc == 3) d = make_uint4(o[3][0], o[3][1], o[3][2], o[3][3]);
+        stage_chunk(tm.scratch, 4 * kq + cc, chunk, d);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::named_barrier(tm.bar, tm.threads);
+      if (t == 0) {
+        ptx::tma_store_2d(&p.map_t, tm.scratch, (int)n0, (int)k0);
+        ptx::bulk_commit();
       }
     }
   }
@@ -559,7 +613,7 @@ struct Q12 {
   static constexpr int kScratchBytes = Q2::kScratchBytes;
   static constexpr uint32_t kTx = kStageBytes;
   static constexpr int kTeams = 2;
-  static constexpr bool kBulkStores = false;
+  static constexpr bool kBulkStores = true;
   static_assert(Q1::kStageBytes == kStageBytes && Q2::kStageBytes == kStageBytes, "tile size");
   static_assert(Q2::kTeams == kTeams && Q2::kTeamWarps == kConsumerWarps / kTeams, "teams");
   struct Params {
@@ -684,32 +738,6 @@ __global__ void tensor_scale_finalize_kernel(float* scale_word) {
 // lanes writes 8 different (k % 8) rows at once, which keeps the writes free
 // of bank conflicts.
 // ---------------------------------------------------------------------------
-
-// 16 bytes into row k, chunk c of a 128 x 128 staging tile (128-byte swizzle).
-__device__ __forceinline__ void stage_chunk(uint8_t* st, int k, int c, uint4 v) {
-  *reinterpret_cast<uint4*>(st + k * 128 + ((c ^ (k & 7)) << 4)) = v;
-}
-
-// The team's staging buffer is free again once the previous tile's bulk
-// stores (issued by the team's thread 0) have read it.
-__device__ __forceinline__ void team_stage_wait(const Team& tm) {
-  if (tm.tid == 0) ptx::bulk_wait_read_all();
-}
-
-// Store the staged tile: codes to (x = m0, y = k0) of the transposed output,
-// and 128 scales to sT_row.  Called by every team thread after its staging
-// writes.
-__device__ __forceinline__ void team_stage_store(const Team& tm, const CUtensorMap* map_out,
-                                                 const uint8_t* st, const float* st_scales,
-                                                 int m0, int k0, float* sT_row) {
-  ptx::fence_proxy_async_smem();
-  ptx::named_barrier(tm.bar, tm.threads);
-  if (tm.tid == 0) {
-    ptx::tma_store_2d(map_out, st, m0, k0);
-    ptx::bulk_store(sT_row, st_scales, 128 * 4);
-    ptx::bulk_commit();
-  }
-}
 
 // Q1T (and, with DUAL, Q1 of the same tile): 128x1 tiles of a bf16
 // activation (128 consecutive rows of one column), written transposed; with
@@ -1113,6 +1141,7 @@ cudaError_t launch_quant_weight_128x128(const void* w, int64_t N, int64_t K, uin
   CUtensorMap map;
   if (!make_tmap_2d(&map, w, 2, N, K, kGroup, kGroup, false)) return cudaErrorInvalidValue;
   Q2::Params p;
+  if (qT && !make_out_map(&p.map_t, qT, K, N)) return cudaErrorInvalidValue;
   p.q = q;
   p.s = s;
   p.qT = qT;
