@@ -49,11 +49,12 @@ FP8_OVER_BF16 = 2.0
 HBM_NOMINAL_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
-# DRAM traffic of one GEMM launch on the dense workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum),
+# DRAM traffic of one GEMM launch on the stress workload from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`,
+# as ncu prints them: 1.19 GB + 257.04 MB),
 # valid only for the kernel code it was taken on (a fingerprint of gemm.cu,
 # ptx.cuh and fp8_common.cuh without comments); null once the code changed.
-TRAFFIC = {"gemm": {"bytes": 87072000 + 35828224, "src_sha": "e666d1eb943cfd55"}}
+TRAFFIC = {"gemm": {"bytes": 1190000000 + 257040000, "src_sha": "79a564694b63f4d4"}}
 
 
 def kernel_source_sha():
@@ -690,6 +691,83 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
     return rows
 
 
+PROFILE_KERNELS = ("q1", "q1t", "dual", "q3", "q2", "q2t", "q1e5", "q3e5", "tensor", "gemm")
+
+
+def profile_kernel(args):
+    """One kernel alone, for ncu: `--warmup` launches, then `--steps` timed
+    launches at the large-K stress tensor (8192 x 16384 bf16, or --shape
+    M,K) with an L2 flush before each.  Prints one JSON line of mean event
+    time and algorithmic rate; this is not a bench line."""
+    import torch
+    import fp8_fine_grained_18_b300 as fp8bs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M, K = (int(v) for v in args.shape.split(",")[:2]) if args.shape else (8192, 16384)
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    a = torch.rand((M, K), generator=g, device=dev).mul_(2).sub_(1).to(torch.bfloat16)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    n_el = M * K
+    k = args.kernel
+    if k == "gemm":
+        b = torch.rand((M, K), generator=g, device=dev).mul_(2).sub_(1).to(torch.bfloat16)
+        qa, sa = fp8bs.quant_act_1x128(a)
+        qb, sb = fp8bs.quant_act_1x128(b)
+        c = torch.empty((M, M), dtype=torch.float32, device=dev)
+        fn = lambda: fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_TILE_1x128, out_dtype=torch.float32, out=c)
+        work, unit = 2.0 * M * M * K / 1e12, "TFLOP/s"
+    else:
+        qa, sa = fp8bs.quant_act_1x128(a)
+        qT, sT = fp8bs.quant_act_1x128(a, transpose_out=True)
+        if k == "q1":
+            fn, nb = (lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa)), algorithmic_bytes_q1(M, K)
+        elif k == "q1t":
+            fn, nb = (lambda: fp8bs.quant_act_1x128(a, transpose_out=True, q=qT, scales=sT)), \
+                algorithmic_bytes_q1(M, K)
+        elif k == "dual":
+            fn, nb = (lambda: fp8bs.quant_act_dual(a, qa, sa, qT, sT)), algorithmic_bytes_dual(M, K)
+        elif k == "q3":
+            fn, nb = (lambda: fp8bs.requant_1x128_to_128x1(qa, sa, qT=qT, scalesT=sT)), \
+                algorithmic_bytes_q3(M, K)
+        elif k in ("q2", "q2t"):
+            qw, sw, qwT, swT = fp8bs.quant_weight_128x128(a, transposed=True)
+            if k == "q2":
+                fn, nb = (lambda: fp8bs.quant_weight_128x128(a, q=qw, scales=sw)), algorithmic_bytes_q2(M, K)
+            else:
+                fn = lambda: fp8bs.quant_weight_128x128(a, transposed=True, q=qw, scales=sw, qT=qwT,
+                                                        scalesT=swT)
+                nb = algorithmic_bytes_q2(M, K, transposed=True)
+        elif k in ("q1e5", "q3e5"):
+            e5 = fp8bs.quant_act_e5m6(a)
+            if k == "q1e5":
+                fn = lambda: fp8bs.quant_act_e5m6(a, packed=e5[0], scales=e5[1], q=e5[2], q_scales=e5[3])
+                nb = int(n_el * (2 + 1 + 1.5 + 8 / 128))
+            else:
+                fn = lambda: fp8bs.requant_e5m6_to_128x1(e5[0], e5[1], qT=qT, scalesT=sT)
+                nb = int(n_el * (1.5 + 1 + 8 / 128))
+        else:
+            qpt, spt, _ = fp8bs.quant_per_tensor(a)
+            fn, nb = (lambda: fp8bs.quant_per_tensor(a, q=qpt, scale=spt)), 3 * n_el + 4
+        work, unit = nb / 1e9, "GB/s"
+    for _ in range(args.warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.mean(times)
+    print(json.dumps({"kernel": k, "shape": [M, K], "launches": args.steps, "ms": round(ms, 4),
+                      "rate": round(work / (ms * 1e-3), 1), "unit": unit}))
+
+
 def cpu_baseline(M, N, K, inp, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the step's workload:
     quantize a few rows of A and of B (1x128) and compute their GEMM block
@@ -784,10 +862,14 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="M,N,K of the step in place of the workload's (profiling)")
     ap.add_argument("--rows-only", default=None, help="time only the rows containing this text")
+    ap.add_argument("--kernel", choices=PROFILE_KERNELS, default=None,
+                    help="profiling: launch only this kernel (see profile_kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.kernel is not None:
+        profile_kernel(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -47,6 +47,7 @@
 // TMEM accumulator and applies K-group 0's scales once at the end: the
 // measurement of what tensor-core-only accumulation costs (P1 paragraph 4).
 #include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include <cuda.h>
@@ -89,8 +90,24 @@ struct Params {
   float* c_scales;  // E4M3 output: [N/128][M]
   int M, N, K, KB;
   int num_m_units, num_units;  // a unit = one 128 x BN tile, or a pair's 256 x BN tile
+  int num_n_units, group_m;     // unit columns; unit rows per group (tile order)
   int skip_iter;
 };
+
+// Unit u's row of units and column of tiles.  Units are taken in groups of
+// group_m unit rows, the row changing fastest within a group: the units in
+// flight at one time then share a few A row panels and B column panels in
+// L2.  With the row changing fastest over all of M, every wave would stream
+// the whole of A from HBM once (measured at the 8192 x 8192 x 16384 stress
+// shape: 2.12 GB read per launch against 0.28 GB of operands).
+__device__ __forceinline__ void unit_coords(const Params& p, int u, int& mu, int& nt) {
+  const int per_group = p.group_m * p.num_n_units;
+  const int grp = u / per_group, r = u - grp * per_group;
+  const int first = grp * p.group_m;
+  const int gm = min(p.num_m_units - first, p.group_m);
+  mu = first + r % gm;
+  nt = r / gm;
+}
 
 // Bounded wait.  Returns false when this wait expired (the error word and
 // the CTA's abort flag get set) or another role already aborted.
@@ -126,13 +143,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // PW promotion warps (8, 12 or 16) share the tile's columns: each owns 32
-// TMEM lanes (rows) and kCols = BN / (PW / 4) columns.  Reading the partials
-// out of TMEM is the promotion's bottleneck: one warp's tcgen05.ld calls run
-// one after another (a 32-column load takes about 180 cycles), and the SM's
-// read rate grows with the number of warps reading at once (measured: about
-// 170 B/clk with two warps per SM sub-partition, 310 with four), against
-// 256 B/clk needed to drain one K-group's partial while the tensor cores
-// compute the next at full rate.
+// TMEM lanes (rows) and kCols = BN / (PW / 4) columns.  The promotion warps'
+// own instruction stream bounds the promoted kernel, not the tensor cores
+// and not the TMEM reads: with the MMAs taken out the 256 x 256 pair runs at
+// the same speed, and a 32-column tcgen05.ld completes in about 20 cycles
+// inside the kernel.  Per K-group each promotion thread spends one FP32
+// operation per element with block B scales and two with per-column B
+// scales (fl(p sb) then fma with sa), which is what separates the two.
 template <int BN, bool PAIR, int PW>
 struct Cfg {
   static constexpr int CM = PAIR ? 2 : 1;  // CTAs per cluster
@@ -417,7 +434,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       uint32_t issued_mask = 0;  // stages with a copy issued at least once
       bool ok = true;
       for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
-        const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
+        int mu, nt;
+        unit_coords(p, u, mu, nt);
+        const int mt = mu * CM + rank;
         for (int kb = 0; kb < KB; ++kb, ++it) {
           const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
           if (!wait_bar(&empty[stage], phase ^ 1, abort_flag, kErrProducer)) { ok = false; break; }
@@ -527,7 +546,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       uint32_t se = 0, sph = 0;  // scale entry and its slot's phase
       bool ok = true;
       for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
-        const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
+        int mu, nt;
+        unit_coords(p, u, mu, nt);
+        const int mt = mu * CM + rank;
         const int m0 = mt * kBM, n0 = nt * BN;
         const int nb_first = n0 / 128;
         const int nb_count = (n0 + BN - 1) / 128 - nb_first + 1;
@@ -592,7 +613,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     uint32_t se = 0, sph = 0;  // scale entry (0 .. kScaleEntries-1) and its slot's phase
     bool ok = true;
     for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
-      const int mt = (u % p.num_m_units) * CM + rank, nt = u / p.num_m_units;
+      int mu, nt;
+      unit_coords(p, u, mu, nt);
+      const int mt = mu * CM + rank;
       const int m0 = mt * kBM, n0 = nt * BN;
       float acc[kCols];
 #pragma unroll
@@ -927,9 +950,19 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   p.num_m_units = (m_tiles + CM - 1) / CM;
   const int n_tiles = (int)((g.N + BN - 1) / BN);
   p.num_units = p.num_m_units * n_tiles;
+  p.num_n_units = n_tiles;
   p.skip_iter = g.skip_iter;
   int units = ki.max_ctas / CM;
   if (units > p.num_units) units = p.num_units;
+  // Group size: the units in flight (about `units`) cover group_m unit rows
+  // and units / group_m tile columns; A bytes grow with the first, B bytes
+  // with the second, and group_m = sqrt(units * BN / unit rows) balances them.
+  {
+    int gm = (int)(sqrtf((float)units * (float)BN / (float)(CM * kBM)) + 0.5f);
+    if (gm < 1) gm = 1;
+    if (gm > p.num_m_units) gm = p.num_m_units;
+    p.group_m = gm;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(units * CM);

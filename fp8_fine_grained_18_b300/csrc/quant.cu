@@ -17,9 +17,11 @@
 // threads must exchange group maxima, the consumers form two teams of 8
 // warps that work on alternate tiles, so one team's barrier waits overlap
 // the other's work.  Tiles are ordered with the K-group fastest, so the CTAs
-// running at one time read one contiguous band of the input.  Q12 and Q1E5
-// are further ops of the same scheme.  Q1T, the dual quantizer and Q3, which
-// transpose, are plain one-tile-per-CTA kernels (see below).  Each
+// running at one time read one contiguous band of the input.  Q12, Q1E5 and
+// the transposing ops (Q1T and the dual quantizer as Q1TS, Q3 and the E5M6
+// re-tiling as Q3S) are further ops of the same scheme: a team stages its
+// transposed codes in a 128-byte-swizzled shared-memory tile that one thread
+// writes out with a tensor store (and the scales with a bulk copy).  Each
 // input byte is read from HBM once and each output byte written once.
 //
 // Group max-abs is an integer max on the sign-stripped bit patterns
