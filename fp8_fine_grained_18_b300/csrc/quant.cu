@@ -755,7 +755,8 @@ struct Q1TS {
   static constexpr bool kBulkStores = true;
   static constexpr int kOffScales = 128 * 128;
   static constexpr int kOffRed = kOffScales + 128 * 4;
-  static constexpr int kScratchBytes = kOffRed + 2 * 4 * 64 * 4;
+  static constexpr int kOffNr = kOffRed + 2 * 4 * 64 * 4;
+  static constexpr int kScratchBytes = kOffNr + 128 * 4;
   static constexpr uint32_t kTx = kStageBytes;
   struct Params {
     CUtensorMap map_out;  // qT [K][M] bytes, 128 x 128 box, 128-byte swizzle (64-byte aligned)
@@ -839,14 +840,38 @@ struct Q1TS {
     red[256 + part * 64 + cp] = mc;
     team_stage_wait(tm);
     ptx::named_barrier(tm.bar, tm.threads);
-    uint32_t mpa = 0, mca = 0;
+    // Each column's scale is made once: team warp tw8 finishes columns
+    // 16 tw8 .. 16 tw8 + 15 (lanes 16..31 repeat lanes 0..15) and writes s
+    // to the scales staging (the previous tile's bulk store has read it) and
+    // -1/s (0 off the fast path) beside it.
+    float* sc = reinterpret_cast<float*>(scr + kOffScales);
+    float* nr = reinterpret_cast<float*>(scr + kOffNr);
+    {
+      const int col = 16 * (t >> 5) + (t & 15), pr = col >> 1, sh = (col & 1) * 16;
+      uint32_t mpa = 0, mca = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mpa = __vmaxu2(mpa, red[q * 64 + cp]);
-      mca = __vmaxu2(mca, red[256 + q * 64 + cp]);
+      for (int q = 0; q < 4; ++q) {
+        mpa = __vmaxu2(mpa, red[q * 64 + pr]);
+        mca = __vmaxu2(mca, red[256 + q * 64 + pr]);
+      }
+      const GroupScale gc = make_scale((mca >> sh) & 0xFFFFu, ((mpa >> sh) & 0xFFFFu) >= kBf16Inf, true);
+      if ((t & 31) < 16) {
+        sc[col] = gc.s;
+        nr[col] = gc.fast ? gc.nr : 0.0f;
+      }
     }
-    const GroupScale glo = make_scale(mca & 0xFFFFu, (mpa & 0xFFFFu) >= kBf16Inf, true);
-    const GroupScale ghi = make_scale(mca >> 16, (mpa >> 16) >= kBf16Inf, true);
+    ptx::named_barrier(tm.bar, tm.threads);
+    GroupScale glo, ghi;
+    {
+      const float2 s2 = *reinterpret_cast<const float2*>(sc + 2 * cp);
+      const float2 n2 = *reinterpret_cast<const float2*>(nr + 2 * cp);
+      glo.s = s2.x;
+      glo.nr = n2.x;
+      glo.fast = n2.x != 0.0f;
+      ghi.s = s2.y;
+      ghi.nr = n2.y;
+      ghi.fast = n2.y != 0.0f;
+    }
     uint32_t olo[8], ohi[8];
 #pragma unroll
     for (int i = 0; i < 32; i += 4) {
@@ -870,8 +895,6 @@ struct Q1TS {
         stage_chunk(scr, k, 2 * part + h, d);
       }
     }
-    float* sc = reinterpret_cast<float*>(scr + kOffScales);
-    if (part == 0) *reinterpret_cast<float2*>(sc + 2 * cp) = make_float2(glo.s, ghi.s);
     team_stage_store(tm, &p.map_out, scr, sc, (int)m0, (int)k0, p.sT + (int64_t)mb * p.K + k0);
   }
 };
@@ -920,7 +943,8 @@ struct Q3S {
   static constexpr bool kBulkStores = true;
   static constexpr int kOffScales = 128 * 128;
   static constexpr int kOffRed = kOffScales + 128 * 4;
-  static constexpr int kScratchBytes = kOffRed + 2 * 8 * 128 * 4;
+  static constexpr int kOffNr = kOffRed + 2 * 8 * 128 * 4;
+  static constexpr int kScratchBytes = kOffNr + 128 * 4;
   static constexpr uint32_t kTx = kStageBytes;
   struct Params {
     CUtensorMap map_out;  // qT [K][M] bytes, 128 x 128 box, 128-byte swizzle (64-byte aligned)
@@ -975,16 +999,38 @@ struct Q3S {
         make_float4(mc[0], mc[1], mc[2], mc[3]);
     team_stage_wait(tm);
     ptx::named_barrier(tm.bar, tm.threads);
-    GroupScale g[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    // Each column's scale is made once: warp `part` finishes columns
+    // 16 part .. 16 part + 15 (lanes 16..31 repeat lanes 0..15) and writes s
+    // to the scales staging (which the previous tile's bulk store has read,
+    // see team_stage_wait) and -1/s (0 off the fast path) beside it.
+    float* sc = reinterpret_cast<float*>(scr + kOffScales);
+    float* nr = reinterpret_cast<float*>(scr + kOffNr);
+    {
+      const int col = 16 * part + (cq & 15);
       float a = 0.0f, b = 0.0f;  // a is NaN if the column holds a NaN
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        a = fmax_abs_nan(a, red[q * 128 + 4 * cq + c]);
-        b = fmaxf(b, red[1024 + q * 128 + 4 * cq + c]);
+        a = fmax_abs_nan(a, red[q * 128 + col]);
+        b = fmaxf(b, red[1024 + q * 128 + col]);
       }
-      g[c] = make_scale(__float_as_uint(b), !(a < __uint_as_float(kF32Inf)), false);
+      const GroupScale gc = make_scale(__float_as_uint(b), !(a < __uint_as_float(kF32Inf)), false);
+      if (cq < 16) {
+        sc[col] = gc.s;
+        nr[col] = gc.fast ? gc.nr : 0.0f;
+      }
+    }
+    ptx::named_barrier(tm.bar, tm.threads);
+    GroupScale g[4];
+    {
+      const float4 s4 = *reinterpret_cast<const float4*>(sc + 4 * cq);
+      const float4 n4 = *reinterpret_cast<const float4*>(nr + 4 * cq);
+      const float sv[4] = {s4.x, s4.y, s4.z, s4.w}, nv[4] = {n4.x, n4.y, n4.z, n4.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        g[c].s = sv[c];
+        g[c].nr = nv[c];
+        g[c].fast = nv[c] != 0.0f;
+      }
     }
     uint32_t o[4][4];
 #pragma unroll
@@ -1011,9 +1057,6 @@ struct Q3S {
       if (cc == 3) d = make_uint4(o[3][0], o[3][1], o[3][2], o[3][3]);
       stage_chunk(scr, 4 * cq + cc, part, d);
     }
-    float* sc = reinterpret_cast<float*>(scr + kOffScales);
-    if (part == 0)
-      *reinterpret_cast<float4*>(sc + 4 * cq) = make_float4(g[0].s, g[1].s, g[2].s, g[3].s);
     team_stage_store(tm, &p.map_out, scr, sc, (int)m0, (int)k0, p.sT + (int64_t)mb * p.K + k0);
   }
 };
