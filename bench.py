@@ -642,6 +642,24 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
               algorithmic_bytes_q2(7168, 2048, transposed=True))
     gemm_row("G1 dgrad 4096x2048x7168 bf16", qdy, sdy, qwT, swT, 0, torch.bfloat16)
     gemm_row("G1 wgrad 7168x2048x4096 f32 (1x128 B scales)", qdyT, sdyT, qxT, sxT, 1, torch.float32)
+    # stream-K: a long-K problem with too few tiles for the SMs (the weight
+    # gradient of a 512-wide layer over 16384 tokens: 4 pair tiles)
+    name = "G1 stream-K 512x512x16384 f32 (1x128 B scales, 4 tiles split over every SM)"
+    if not skip(name):
+        Ms, Ks = 512, 16384
+        qs_a, ss_a = fp8bs.quant_act_1x128(bf(synth.normal(np.random.default_rng(9), (Ms, Ks), 1.0)))
+        qs_b, ss_b = fp8bs.quant_act_1x128(bf(synth.normal(np.random.default_rng(10), (Ms, Ks), 1e-3)))
+        need = fp8bs.gemm_streamk_workspace(Ms, Ms, Ks, 1, torch.float32)
+        wsp = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        cs = torch.empty((Ms, Ms), dtype=torch.float32, device=dev)
+        ms_sk, n_sk, clk = timed(lambda: fp8bs.gemm_streamk(qs_a, ss_a, qs_b, ss_b, 1, out_dtype=torch.float32,
+                                                             workspace=wsp if need else None, out=cs))
+        ms_wt, _, _ = timed(lambda: fp8bs.gemm(qs_a, ss_a, qs_b, ss_b, 1, out_dtype=torch.float32, out=cs))
+        tf = 2.0 * Ms * Ms * Ks / (ms_sk * 1e-3) / 1e12
+        rows[name] = {"M": Ms, "N": Ms, "K": Ks, "ms": round(ms_sk, 4), "TFLOP/s": round(tf, 1),
+                      "frac_fp8_peak": round(tf / fp8_peak, 4), "whole_tiles_ms": round(ms_wt, 4),
+                      "workspace_bytes": need, "launches": n_sk, "clocks": clk}
+        del qs_a, ss_a, qs_b, ss_b, wsp, cs
     del x, wt, dy, qx, sx, qxT, sxT, qdyT, sdyT, qdy, sdy, qw, sw, qwT, swT
 
     # every quantizer at the bandwidth shape 8192 x 16384 (the stress A

@@ -48,6 +48,8 @@ _SIGS = {
     "fp8bs_gemm_ex": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _P],
     "fp8bs_gemm_tiled": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _I, _I, _P],
     "fp8bs_gemm_quant_out": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P],
+    "fp8bs_gemm_streamk_workspace": [_I, _I64, _I64, _I64, _I, _P],
+    "fp8bs_gemm_streamk": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, ctypes.c_size_t, _P],
     "fp8bs_debug_gemm_stall": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I, _I, _P],
     "fp8bs_get_device_error": [_P],
     "fp8bs_status_string": [_I],
@@ -236,6 +238,39 @@ def gemm(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
     _check(_lib.fp8bs_gemm_tiled(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K,
                                  _ptr(c), odt, int(bool(promote)), int(tile), _stream(a)),
            "fp8bs_gemm")
+    return c
+
+
+def gemm_streamk_workspace(M: int, N: int, K: int, bkind: int = BSCALE_BLOCK_128x128,
+                           out_dtype=torch.bfloat16) -> int:
+    """Workspace bytes gemm_streamk needs for this problem on the current
+    device (0: it runs as gemm)."""
+    n = ctypes.c_size_t(0)
+    odt = OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32
+    _check(_lib.fp8bs_gemm_streamk_workspace(int(bkind), M, N, K, odt, ctypes.addressof(n)),
+           "fp8bs_gemm_streamk_workspace")
+    return n.value
+
+
+def gemm_streamk(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
+                 bkind: int = BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, workspace=None,
+                 out=None):
+    """gemm (promoted) with stream-K scheduling of an uneven last wave.
+    workspace: a uint8 CUDA tensor of at least gemm_streamk_workspace bytes
+    (allocated here when None)."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8
+    M, K = a.shape
+    N = b.shape[0]
+    odt = OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32
+    c = _empty((M, N), out_dtype, a) if out is None else out
+    if workspace is None:
+        need = gemm_streamk_workspace(M, N, K, bkind, out_dtype)
+        workspace = _empty((max(need, 1),), torch.uint8, a) if need else None
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() if workspace is not None else 0
+    _check(_lib.fp8bs_gemm_streamk(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K,
+                                   _ptr(c), odt, ws_ptr, ws_bytes, _stream(a)),
+           "fp8bs_gemm_streamk")
     return c
 
 

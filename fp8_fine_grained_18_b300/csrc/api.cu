@@ -60,7 +60,8 @@ bool transposed_shape_ok(int64_t M, int64_t K) {
 fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, const float* sb,
                          fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K, void* c,
                          fp8bs_out_dtype out, int promote, int skip_iter, int tile,
-                         fp8bs_stream_t stream, float* c_scales = nullptr) {
+                         fp8bs_stream_t stream, float* c_scales = nullptr, void* ws = nullptr,
+                         size_t ws_bytes = 0) {
   if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
   if (bkind != FP8BS_BSCALE_BLOCK_128x128 && bkind != FP8BS_BSCALE_TILE_1x128)
     return FP8BS_ERR_INVALID_ARG;
@@ -94,7 +95,52 @@ fp8bs_status gemm_common(const uint8_t* a, const float* sa, const uint8_t* b, co
   g.promote = promote != 0;
   g.skip_iter = skip_iter;
   g.tile = tile;
+  if (ws != nullptr) {
+    size_t need = 0;
+    g.ws_need = &need;
+    fp8bs_status qs = cuda_status(fp8bs::launch_gemm(g, as_cuda(stream)));
+    if (qs != FP8BS_OK) return qs;
+    if (ws_bytes < need) return FP8BS_ERR_INVALID_ARG;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FP8BS_ERR_MISALIGNED;
+    g.ws_need = nullptr;
+    g.ws = ws;
+    g.ws_bytes = ws_bytes;
+  }
   return cuda_status(fp8bs::launch_gemm(g, as_cuda(stream)));
+}
+
+// Workspace bytes of the stream-K GEMM for this problem on the current
+// device (shape checks as gemm_common; no pointers needed).
+fp8bs_status streamk_need(fp8bs_bscale_kind bkind, int64_t M, int64_t N, int64_t K,
+                          fp8bs_out_dtype out, size_t* bytes) {
+  if (!bytes) return FP8BS_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (M < 0 || N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+  if (bkind != FP8BS_BSCALE_BLOCK_128x128 && bkind != FP8BS_BSCALE_TILE_1x128)
+    return FP8BS_ERR_INVALID_ARG;
+  if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FP8BS_OK;
+  if (K == 0 || K % 128 != 0 || N % 16 != 0) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  fp8bs_status st = check_device();
+  if (st != FP8BS_OK) return st;
+  fp8bs::GemmArgs g;
+  g.a = nullptr;
+  g.sa = nullptr;
+  g.b = nullptr;
+  g.sb = nullptr;
+  g.b_tile = bkind == FP8BS_BSCALE_TILE_1x128;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.c = nullptr;
+  g.c_scales = nullptr;
+  g.out = out == FP8BS_OUT_BF16 ? 1 : 0;
+  g.promote = true;
+  g.skip_iter = -1;
+  g.tile = FP8BS_TILE_AUTO;
+  g.ws_need = bytes;
+  return cuda_status(fp8bs::launch_gemm(g, nullptr));
 }
 
 }  // namespace
@@ -261,6 +307,28 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t* a, const float* sa, const uint8_t* 
                               int64_t K, void* c, fp8bs_out_dtype out, int promote,
                               fp8bs_tile_shape tile, fp8bs_stream_t stream) {
   return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, promote, -1, tile, stream);
+}
+
+fp8bs_status fp8bs_gemm_streamk_workspace(fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                                          int64_t K, fp8bs_out_dtype out, size_t* bytes) {
+  return streamk_need(bkind, M, N, K, out, bytes);
+}
+
+fp8bs_status fp8bs_gemm_streamk(const uint8_t* a, const float* sa, const uint8_t* b,
+                                const float* sb, fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                                int64_t K, void* c, fp8bs_out_dtype out, void* workspace,
+                                size_t workspace_bytes, fp8bs_stream_t stream) {
+  if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+  if (workspace == nullptr && workspace_bytes != 0) return FP8BS_ERR_INVALID_ARG;
+  if (workspace == nullptr) {
+    // no workspace: valid only where the plan needs none
+    size_t need = 0;
+    fp8bs_status st = streamk_need(bkind, M, N, K, out, &need);
+    if (st != FP8BS_OK) return st;
+    if (need > 0) return FP8BS_ERR_INVALID_ARG;
+  }
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, 1, -1, FP8BS_TILE_AUTO, stream,
+                     nullptr, workspace, workspace_bytes);
 }
 
 fp8bs_status fp8bs_gemm_quant_out(const uint8_t* a, const float* sa, const uint8_t* b,

@@ -92,6 +92,17 @@ struct Params {
   int num_m_units, num_units;  // a unit = one 128 x BN tile, or a pair's 256 x BN tile
   int num_n_units, group_m;     // unit columns; unit rows per group (tile order)
   int skip_iter;
+  // Stream-K: units below sk_begin go whole to CTA groups g, g + G, ...
+  // (G = num_groups); the S = sk_iters K-groups of units sk_begin..
+  // (unit-major) are split evenly: with S = q G + r (sk_q, sk_r), group g
+  // takes q + 1 of them if g < r, else q, in group order.  A unit split over
+  // several groups is summed through ws (each group's FP32 share) and ws_cnt
+  // (one arrival counter per unit, CTA and promotion warp); sk_begin ==
+  // num_units turns it off.
+  int sk_begin, num_groups;
+  int sk_iters, sk_q, sk_r;
+  float* ws;
+  unsigned int* ws_cnt;
 };
 
 // Unit u's row of units and column of tiles.  Units are taken in groups of
@@ -107,6 +118,66 @@ __device__ __forceinline__ void unit_coords(const Params& p, int u, int& mu, int
   const int gm = min(p.num_m_units - first, p.group_m);
   mu = first + r % gm;
   nt = r / gm;
+}
+
+// First stream-K iteration of CTA group g's share.
+__device__ __forceinline__ int sk_share_begin(const Params& p, int g) {
+  return g * p.sk_q + min(g, p.sk_r);
+}
+
+// The CTA group whose share holds stream-K iteration `it`.
+__device__ __forceinline__ int sk_owner(const Params& p, int it) {
+  const int big = p.sk_r * (p.sk_q + 1);  // iterations of the r larger shares
+  return it < big ? it / (p.sk_q + 1) : p.sk_r + (it - big) / p.sk_q;
+}
+
+// The work of CTA group g, one item at a time: whole units g, g + G, ...
+// below sk_begin, then its stream-K share as segments (unit u, K-groups
+// kb0 .. kb1 - 1).  Every role of the CTA walks the same items.
+struct WorkIter {
+  int u, kb0, kb1;
+  int it, it_end;
+  bool valid;
+  __device__ __forceinline__ WorkIter(const Params& p, int g) {
+    u = g;
+    kb0 = 0;
+    kb1 = p.KB;
+    it = sk_share_begin(p, g);
+    it_end = sk_share_begin(p, g + 1);
+    valid = true;
+    if (u >= p.sk_begin) start_sk(p);
+  }
+  __device__ __forceinline__ void start_sk(const Params& p) {
+    valid = it < it_end;
+    if (!valid) return;
+    u = p.sk_begin + it / p.KB;
+    kb0 = it % p.KB;
+    kb1 = min(p.KB, kb0 + (it_end - it));
+  }
+  __device__ __forceinline__ void next(const Params& p) {
+    if (u < p.sk_begin) {
+      u += p.num_groups;
+      kb0 = 0;
+      kb1 = p.KB;
+      if (u >= p.sk_begin) start_sk(p);
+      return;
+    }
+    it += kb1 - kb0;
+    start_sk(p);
+  }
+  // true when this is the group's last item
+  __device__ __forceinline__ bool last(const Params& p) const {
+    WorkIter n = *this;
+    n.next(p);
+    return !n.valid;
+  }
+};
+
+// Workspace slot of group g's segment of unit u: 2 g for the first segment
+// of g's stream-K share, 2 g + 1 for its last (a share holds at most these
+// two partial segments; whole units between them need no slot).
+__device__ __forceinline__ int sk_slot(const Params& p, int g, int u) {
+  return u == p.sk_begin + sk_share_begin(p, g) / p.KB ? 2 * g : 2 * g + 1;
 }
 
 // Bounded wait.  Returns false when this wait expired (the error word and
@@ -317,6 +388,60 @@ __device__ __forceinline__ void promote_step(float* acc, const uint32_t* v, floa
   }
 }
 
+// A promotion warp's FP32 share of a stream-K unit in the workspace: lane
+// l's columns j .. j+3 at float4 l + 32 (j / 4) of the warp's chunk, so each
+// store or load of the warp covers 512 contiguous bytes.  One base address
+// and immediate offsets, and the loads one at a time (ordered volatile asm,
+// each sum pinned before the next load): the share needs no registers
+// beside the accumulator.
+template <int kCols, int J = 0>
+__device__ __forceinline__ void share_store(const float4* base, const float* acc) {
+  if constexpr (J < kCols) {
+    asm volatile("st.global.cg.v4.f32 [%0+%1], {%2, %3, %4, %5};" ::"l"(base), "n"(J / 4 * 512),
+                 "f"(acc[J]), "f"(acc[J + 1]), "f"(acc[J + 2]), "f"(acc[J + 3])
+                 : "memory");
+    share_store<kCols, J + 4>(base, acc);
+  }
+}
+
+// acc[J .. J+31] = the sum over groups g_first .. g_last, in that order, of
+// their shares' float4s J / 4 .. J / 4 + 7 (sh(g) gives a group's base
+// address): eight loads in flight per group, the batch's sums pinned before
+// the next batch's loads so that at most 64 registers join the accumulator.
+template <int kCols, int J = 0, class Sh>
+__device__ __forceinline__ void share_sum(float* acc, const Sh& sh, int g_first, int g_last) {
+  if constexpr (J < kCols) {
+    constexpr int kB = (kCols - J) / 4 < 8 ? (kCols - J) / 4 : 8;  // float4s in this batch
+    float4 t[kB];
+#pragma unroll
+    for (int i = 0; i < kB; ++i) t[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 1
+    for (int g = g_first; g <= g_last; ++g) {
+      const float4* base = sh(g);
+      float4 v[kB];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) v[i] = __ldcg(base + (J / 4 + i) * 32);
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        t[i].x += v[i].x;
+        t[i].y += v[i].y;
+        t[i].z += v[i].z;
+        t[i].w += v[i].w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      acc[J + 4 * i] = t[i].x;
+      acc[J + 4 * i + 1] = t[i].y;
+      acc[J + 4 * i + 2] = t[i].z;
+      acc[J + 4 * i + 3] = t[i].w;
+      asm volatile("" : "+f"(acc[J + 4 * i]), "+f"(acc[J + 4 * i + 1]), "+f"(acc[J + 4 * i + 2]),
+                   "+f"(acc[J + 4 * i + 3]));
+    }
+    share_sum<kCols, J + 4 * kB>(acc, sh, g_first, g_last);
+  }
+}
+
 // Load kC columns (32 or 16) from TMEM.
 template <int kC>
 __device__ __forceinline__ void tmem_ld_step(uint32_t taddr, uint32_t* r) {
@@ -417,8 +542,7 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int KB = p.KB;
-  const int unit_first = blockIdx.x / CM;
-  const int unit_stride = gridDim.x / CM;
+  const int unit_first = blockIdx.x / CM;  // this CTA's group
 
   if (warp < kFirstPromoWarp) {
   // Warpgroup 0: producer, MMA issuer, scale loader (warp 3 idles).  Each
@@ -433,11 +557,11 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       uint32_t it = 0;
       uint32_t issued_mask = 0;  // stages with a copy issued at least once
       bool ok = true;
-      for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+      for (WorkIter wk(p, unit_first); ok && wk.valid; wk.next(p)) {
         int mu, nt;
-        unit_coords(p, u, mu, nt);
+        unit_coords(p, wk.u, mu, nt);
         const int mt = mu * CM + rank;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
           const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
           if (!wait_bar(&empty[stage], phase ^ 1, abort_flag, kErrProducer)) { ok = false; break; }
           if ((int)it == p.skip_iter) continue;  // test hook: never arrives
@@ -480,9 +604,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     if (lane == 0 && (!PAIR || rank == 0)) {
       uint32_t it = 0, kt = 0;
       bool ok = true;
-      for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+      for (WorkIter wk(p, unit_first); ok && wk.valid; wk.next(p)) {
         if (PROMOTE) {
-          for (int kb = 0; kb < KB; ++kb, ++it, ++kt) {
+          for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it, ++kt) {
             // The operands usually land long before the TMEM buffer comes
             // back: wait for them first, so that once the promotion warps
             // release the buffer only the MMAs remain to be issued.
@@ -512,13 +636,13 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
           if (!wait_bar(&tempty[buf], tph ^ 1, abort_flag, kErrMma)) break;
           ptx::tc_fence_after();
           const uint32_t d = tmem_base + buf * L::kTmemStride;
-          for (int kb = 0; kb < KB; ++kb, ++it) {
+          for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
             const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1;
             if (!wait_bar(&full[stage], phase, abort_flag, kErrMma)) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_addr(sA + stage * L::kABytes);
             const uint32_t b0 = ptx::smem_addr(sB + stage * L::kBBytes);
-            issue_kgroup<PAIR>(d, a0, b0, kIdesc, kb > 0);
+            issue_kgroup<PAIR>(d, a0, b0, kIdesc, kb > wk.kb0);
             commit_stage<PAIR>(&empty[stage]);
           }
           if (!ok) break;
@@ -545,16 +669,16 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     if (PROMOTE) {
       uint32_t se = 0, sph = 0;  // scale entry and its slot's phase
       bool ok = true;
-      for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+      for (WorkIter wk(p, unit_first); ok && wk.valid; wk.next(p)) {
         int mu, nt;
-        unit_coords(p, u, mu, nt);
+        unit_coords(p, wk.u, mu, nt);
         const int mt = mu * CM + rank;
         const int m0 = mt * kBM, n0 = nt * BN;
         const int nb_first = n0 / 128;
         const int nb_count = (n0 + BN - 1) / 128 - nb_first + 1;
-        const int kb_close = u + unit_stride >= p.num_units ? KB - 1 : KB;
+        const int kb_close = wk.last(p) ? wk.kb1 - 1 : KB;
 #pragma unroll 1
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           const uint32_t slot = se / kScaleGroup, sub = se % kScaleGroup;
           if (sub == 0) {
             bool w = wait_bar(&sempty[slot], sph ^ 1, abort_flag, kErrScales);
@@ -612,7 +736,8 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     uint32_t kt = 0;
     uint32_t se = 0, sph = 0;  // scale entry (0 .. kScaleEntries-1) and its slot's phase
     bool ok = true;
-    for (int u = unit_first; ok && u < p.num_units; u += unit_stride) {
+    for (WorkIter wk(p, unit_first); ok && wk.valid; wk.next(p)) {
+      const int u = wk.u;
       int mu, nt;
       unit_coords(p, u, mu, nt);
       const int mt = mu * CM + rank;
@@ -645,9 +770,9 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         };
         uint32_t v[2][32];
         // the CTA's last K-group closes its scale slot early
-        const int kb_close = u + unit_stride >= p.num_units ? KB - 1 : KB;
+        const int kb_close = wk.last(p) ? wk.kb1 - 1 : KB;
 #pragma unroll 1
-        for (int kb = 0; kb < KB; ++kb, ++kt) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++kt) {
           const uint32_t buf = kt % TBUF, tph = (kt / TBUF) & 1;
           const uint32_t slot = se / kScaleGroup, sub = se % kScaleGroup;
           const float* sc = sScale + se * L::kScaleFloats;
@@ -767,6 +892,37 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         ++kt;
       }
       if (!ok) break;
+
+      if (PROMOTE && OUT != kOutE4m3 && (wk.kb0 != 0 || wk.kb1 != KB)) {
+        // A stream-K unit split over CTA groups g_first .. g_last.  Every
+        // share goes to the workspace (this warp's 32 rows x kCols, laid out
+        // so that each float4 store of the warp covers 512 contiguous bytes),
+        // then an arrival counter per (unit, CTA, warp) picks the last
+        // arriver, which sums the shares in K order and writes the tile.
+        const int tsk = u - p.sk_begin;
+        const int t_it0 = tsk * KB;
+        const int g_first = sk_owner(p, t_it0), g_last = sk_owner(p, t_it0 + KB - 1);
+        const size_t chunk = (size_t)32 * kCols / 4;  // float4s per warp share
+        auto share = [&](int g) {
+          return reinterpret_cast<float4*>(p.ws) +
+                 (((size_t)sk_slot(p, g, u) * CM + rank) * kPromoWarps + w) * chunk;
+        };
+        // one base address per share, each float4 at an immediate offset
+        const float4* mine = share(unit_first) + lane;
+        share_store<kCols>(mine, acc);
+        __threadfence();
+        __syncwarp();
+        unsigned int* cnt = p.ws_cnt + ((size_t)tsk * CM + rank) * kPromoWarps + w;
+        unsigned int ticket = 0;
+        if (lane == 0) ticket = atomicAdd(cnt, 1u);
+        ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+        if ((int)ticket != g_last - g_first) continue;  // another group finishes the unit
+        __threadfence();
+        // every share, this group's included, read back in K order: acc =
+        // ((share_first + share_next) + ...) whichever group arrives last
+        share_sum<kCols>(acc, [&](int g) { return share(g) + lane; }, g_first, g_last);
+        if (lane == 0) *cnt = 0u;  // ready for the next launch
+      }
 
       // ---- epilogue: registers -> global (bf16 RNE or fp32)
       const int m = m0 + row;
@@ -934,6 +1090,37 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   }
   if (ki.err != cudaSuccess) return ki.err;
 
+  // Stream-K plan.  When whole units would keep the CTA groups busy less
+  // than 60% of the time (few units for the groups: e.g. 16 pair tiles on
+  // 74 pairs), the units of the last two waves (all of them, below two
+  // waves) have their K-groups spread evenly over every group.  Above that,
+  // the shares' hand-off through the workspace costs more than the idle
+  // groups (measured: 128 tiles on 74 pairs, 86% busy, ran 12% slower
+  // split).  Workspace:
+  // two FP32 shares of a CTA's 128 x BN accumulator per group (the partial
+  // first and last segments of its share), then one arrival counter per
+  // stream-K unit, CTA and promotion warp.
+  const int64_t m_units = ((g.M + kBM - 1) / kBM + CM - 1) / CM;
+  const int64_t all_units = m_units * ((g.N + BN - 1) / BN);
+  const int64_t groups = ki.max_ctas / CM;
+  int64_t sk_begin = all_units;
+  size_t ws_shares = 0, ws_need = 0;
+  if (PROMOTE && OUT != kOutE4m3 && (g.ws != nullptr || g.ws_need != nullptr) && groups > 0) {
+    const int64_t waves = (all_units + groups - 1) / groups;
+    // (the stream-K iteration count must fit an int)
+    const int64_t sk_units_max = all_units / groups >= 1 ? all_units % groups + groups : all_units;
+    if (10 * all_units < 6 * waves * groups && sk_units_max * (g.K / kBK) < (int64_t(1) << 31)) {
+      sk_begin = all_units / groups >= 1 ? (all_units / groups - 1) * groups : 0;
+      ws_shares = (size_t)2 * groups * CM * kBM * BN * sizeof(float);
+      ws_need = ws_shares + (size_t)(all_units - sk_begin) * CM * PW * sizeof(unsigned int);
+    }
+  }
+  if (g.ws_need != nullptr) {
+    *g.ws_need = ws_need;
+    return cudaSuccess;
+  }
+  if (ws_need > g.ws_bytes) return cudaErrorInvalidValue;
+
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, g.a, g.M, g.K, kBM) || !make_tmap(&tb, g.b, g.N, g.K, L::kBH))
     return cudaErrorInvalidValue;
@@ -953,7 +1140,22 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   p.num_n_units = n_tiles;
   p.skip_iter = g.skip_iter;
   int units = ki.max_ctas / CM;
-  if (units > p.num_units) units = p.num_units;
+  if (units > p.num_units && ws_need == 0) units = p.num_units;
+  p.num_groups = units;
+  p.sk_begin = (int)sk_begin;
+  p.sk_iters = (int)((all_units - sk_begin) * p.KB);
+  p.sk_q = p.sk_iters / units;
+  p.sk_r = p.sk_iters % units;
+  p.ws = nullptr;
+  p.ws_cnt = nullptr;
+  if (ws_need > 0) {
+    p.ws = static_cast<float*>(g.ws);
+    p.ws_cnt = reinterpret_cast<unsigned int*>(static_cast<char*>(g.ws) + ws_shares);
+    // the counters start every launch at zero (a launch that timed out may
+    // have left some behind)
+    e = cudaMemsetAsync(p.ws_cnt, 0, ws_need - ws_shares, stream);
+    if (e != cudaSuccess) return e;
+  }
   // Group size: the units in flight (about `units`) cover group_m unit rows
   // and units / group_m tile columns; A bytes grow with the first, B bytes
   // with the second, and group_m = sqrt(units * BN / unit rows) balances them.

@@ -54,6 +54,13 @@ struct GemmArgs {
   bool promote;
   int skip_iter;  // test hook: producer skips this pipeline iteration (-1: never)
   int tile;       // fp8bs_tile_shape value; -1 chooses per problem shape
+  // Stream-K workspace (device memory, 256-byte aligned) and its size; null
+  // runs every unit whole.  With ws_need set, nothing is launched: the
+  // workspace bytes this problem needs are written there (0: stream-K is not
+  // used for it).
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  size_t* ws_need = nullptr;
 };
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);

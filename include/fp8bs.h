@@ -52,6 +52,7 @@
 #ifndef FP8BS_H
 #define FP8BS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -225,6 +226,41 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *a, const float *sa,
                               int64_t K, void *c, fp8bs_out_dtype out,
                               int promote, fp8bs_tile_shape tile,
                               fp8bs_stream_t stream);
+
+/*
+ * fp8bs_gemm (promoted, every 128 K [P1¶3]) with stream-K scheduling for
+ * problems with too few output tiles for the SMs (long K, small M x N):
+ * when whole tiles would keep the SMs busy less than 60% of the time, the
+ * K-groups of the last two waves' tiles (all tiles, below two waves) are
+ * spread evenly over every SM.  A tile split over several SMs is completed by the last
+ * of them to finish: each writes its FP32 share of the tile to the
+ * workspace, and the last sums the shares in K order (so the result does
+ * not depend on which finishes last; it may differ from fp8bs_gemm's by
+ * FP32 rounding, within the same tolerance) and writes C.
+ * Other problems run exactly as fp8bs_gemm.
+ *
+ * fp8bs_gemm_streamk_workspace writes to *bytes the workspace size this
+ * problem needs on the current device (0: no workspace, stream-K not used).
+ * It launches nothing.  out: FP32 or BF16 only.
+ *
+ * fp8bs_gemm_streamk: arguments and layouts as fp8bs_gemm; workspace is
+ * caller-owned device memory of at least that many bytes, 256-byte aligned
+ * (FP8BS_ERR_MISALIGNED otherwise), not read or written by anything else
+ * until the call's stream work is done.  Its contents need no
+ * initialisation: the call zeroes the arrival counters on `stream` before
+ * the GEMM.  A null workspace is accepted only when the problem needs none.
+ * A workspace smaller than needed returns FP8BS_ERR_INVALID_ARG before any
+ * launch.  Two calls in flight on one workspace race.
+ */
+fp8bs_status fp8bs_gemm_streamk_workspace(fp8bs_bscale_kind bkind, int64_t M,
+                                          int64_t N, int64_t K,
+                                          fp8bs_out_dtype out, size_t *bytes);
+fp8bs_status fp8bs_gemm_streamk(const uint8_t *a, const float *sa,
+                                const uint8_t *b, const float *sb,
+                                fp8bs_bscale_kind bkind, int64_t M, int64_t N,
+                                int64_t K, void *c, fp8bs_out_dtype out,
+                                void *workspace, size_t workspace_bytes,
+                                fp8bs_stream_t stream);
 
 /*
  * Both operands of the forward GEMM quantized in one launch [P1¶3]: the
