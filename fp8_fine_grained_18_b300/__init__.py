@@ -50,6 +50,7 @@ _SIGS = {
     "fp8bs_gemm_quant_out": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P],
     "fp8bs_gemm_streamk_workspace": [_I, _I64, _I64, _I64, _I, _P],
     "fp8bs_gemm_streamk": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P, ctypes.c_size_t, _P],
+    "fp8bs_gemm_streamk_noalloc": [_P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _I, _P],
     "fp8bs_debug_gemm_stall": [_P, _P, _P, _P, _I64, _I64, _I64, _P, _I, _I, _P],
     "fp8bs_get_device_error": [_P],
     "fp8bs_status_string": [_I],
@@ -271,6 +272,21 @@ def gemm_streamk(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.T
     _check(_lib.fp8bs_gemm_streamk(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N, K,
                                    _ptr(c), odt, ws_ptr, ws_bytes, _stream(a)),
            "fp8bs_gemm_streamk")
+    return c
+
+
+def gemm_streamk_noalloc(a: torch.Tensor, sa: torch.Tensor, b: torch.Tensor, sb: torch.Tensor,
+                         bkind: int = BSCALE_BLOCK_128x128, out_dtype=torch.bfloat16, out=None):
+    """gemm_streamk on the library's fixed scratch (fp8bs_gemm_streamk_noalloc):
+    no workspace argument; see include/fp8bs.h for its limit and set-up."""
+    assert a.dtype == torch.uint8 and b.dtype == torch.uint8
+    M, K = a.shape
+    N = b.shape[0]
+    odt = OUT_BF16 if out_dtype == torch.bfloat16 else OUT_F32
+    c = _empty((M, N), out_dtype, a) if out is None else out
+    _check(_lib.fp8bs_gemm_streamk_noalloc(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), int(bkind), M, N,
+                                           K, _ptr(c), odt, _stream(a)),
+           "fp8bs_gemm_streamk_noalloc")
     return c
 
 

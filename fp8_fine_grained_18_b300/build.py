@@ -18,7 +18,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libfp8bs.so")
 HEADER = os.path.join(ROOT, "include", "fp8bs.h")
 
-SOURCES = ["api.cu", "tmap.cu", "quant.cu", "gemm.cu"]
+SOURCES = ["api.cu", "tmap.cu", "quant.cu", "gemm.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

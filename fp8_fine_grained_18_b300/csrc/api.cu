@@ -331,6 +331,25 @@ fp8bs_status fp8bs_gemm_streamk(const uint8_t* a, const float* sa, const uint8_t
                      nullptr, workspace, workspace_bytes);
 }
 
+fp8bs_status fp8bs_gemm_streamk_noalloc(const uint8_t* a, const float* sa, const uint8_t* b,
+                                        const float* sb, fp8bs_bscale_kind bkind, int64_t M,
+                                        int64_t N, int64_t K, void* c, fp8bs_out_dtype out,
+                                        fp8bs_stream_t stream) {
+  if (out != FP8BS_OUT_BF16 && out != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+  size_t need = 0;
+  fp8bs_status st = streamk_need(bkind, M, N, K, out, &need);
+  if (st != FP8BS_OK) return st;
+  if (need > fp8bs::noalloc_scratch_bytes()) return FP8BS_ERR_UNSUPPORTED_SHAPE;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (need > 0) {
+    cudaError_t e = fp8bs::noalloc_scratch(&ws, &ws_bytes);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return gemm_common(a, sa, b, sb, bkind, M, N, K, c, out, 1, -1, FP8BS_TILE_AUTO, stream,
+                     nullptr, ws, ws_bytes);
+}
+
 fp8bs_status fp8bs_gemm_quant_out(const uint8_t* a, const float* sa, const uint8_t* b,
                                    const float* sb, fp8bs_bscale_kind bkind, int64_t M, int64_t N,
                                    int64_t K, uint8_t* c, float* c_scales,

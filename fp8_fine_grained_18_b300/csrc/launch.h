@@ -65,6 +65,11 @@ struct GemmArgs {
 
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
+// The fixed scratch of fp8bs_gemm_streamk_noalloc on the current device (its
+// address is looked up once per device) and its size.
+cudaError_t noalloc_scratch(void** ptr, size_t* bytes);
+size_t noalloc_scratch_bytes();
+
 // Enqueue on `stream` a one-thread kernel that atomically exchanges the
 // device error word of the bounded waits in the GEMM (or in the quantizers)
 // with 0 and writes the old value to *dst (device-visible memory, e.g. a

@@ -263,6 +263,40 @@ fp8bs_status fp8bs_gemm_streamk(const uint8_t *a, const float *sa,
                                 fp8bs_stream_t stream);
 
 /*
+ * fp8bs_gemm_streamk for callers that cannot allocate device memory: a
+ * plain C host program with no device allocator of its own, or a runtime
+ * that must not allocate once it is running (cudaMalloc can synchronize the
+ * device and can fail under memory pressure).  The pages have no
+ * counterpart to this call: it is a convenience of this library's API.
+ * Arguments, layouts, result and error codes as fp8bs_gemm_streamk, without
+ * the workspace: the stream-K shares and arrival counters live in one fixed
+ * array of FP8BS_NOALLOC_SCRATCH_BYTES in the library's device memory, one
+ * per device.  Nothing is allocated by the call.
+ *   - A problem whose stream-K plan needs more scratch than that returns
+ *     FP8BS_ERR_UNSUPPORTED_SHAPE before any launch
+ *     (fp8bs_gemm_streamk_workspace gives the need).  Problems that plan no
+ *     stream-K need none and run as fp8bs_gemm.
+ *   - Nothing has to be zeroed by the caller: the array is zero when the
+ *     library's module loads, the call zeroes the arrival counters on
+ *     `stream` before each launch, and every share is written before it is
+ *     read.
+ *   - Set-up: the first call on each device that needs scratch looks up the
+ *     array's address on that device (cudaGetSymbolAddress, with the device
+ *     current) and may load the module; make that first call before
+ *     beginning any stream capture.
+ *   - One array per device: two calls in flight on one device (other
+ *     streams, other host threads) race on it.  Order them on one stream or
+ *     synchronize between them.
+ */
+#define FP8BS_NOALLOC_SCRATCH_BYTES (32u << 20)
+fp8bs_status fp8bs_gemm_streamk_noalloc(const uint8_t *a, const float *sa,
+                                        const uint8_t *b, const float *sb,
+                                        fp8bs_bscale_kind bkind, int64_t M,
+                                        int64_t N, int64_t K, void *c,
+                                        fp8bs_out_dtype out,
+                                        fp8bs_stream_t stream);
+
+/*
  * Both operands of the forward GEMM quantized in one launch [P1¶3]: the
  * activation x in 1x128 tiles (exactly fp8bs_quant_act_1x128 with
  * transpose_out = 0) and the weight w in 128x128 blocks (exactly
