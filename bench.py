@@ -50,11 +50,10 @@ HBM_NOMINAL_GBS = 8000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM traffic of one GEMM launch on the stress workload from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`,
-# as ncu prints them: 1.19 GB + 257.04 MB),
+# (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`),
 # valid only for the kernel code it was taken on (a fingerprint of gemm.cu,
 # ptx.cuh and fp8_common.cuh without comments); null once the code changed.
-TRAFFIC = {"gemm": {"bytes": 1190000000 + 257040000, "src_sha": "79a564694b63f4d4"}}
+TRAFFIC = {"gemm": {"bytes": 1189381632 + 257572864, "src_sha": "e65d3684ec1a5b57"}}
 
 
 def kernel_source_sha():
