@@ -258,14 +258,21 @@ struct Cfg {
   static constexpr int kBBytes = kBH * kBK;
   static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
   static constexpr int kScaleFloats = kBM + kScaleB;
+  // Epilogue staging for tensor-store output: 4 KB per promotion warp (its
+  // 32 rows x 128 bytes), when the warp's columns are whole 32-column chunks.
+  static constexpr bool kEpiTma = kCols % 32 == 0;
+  static constexpr int kEpiBytes = kEpiTma ? PW * 4096 : 0;
   static constexpr int kNumBarsMax = 2 * 8 + 2 * 4 + 2 * kScaleSlots + 1;
-  static constexpr int kFixed = kScaleEntries * kScaleFloats * 4 + kNumBarsMax * 8 + 16 + 1024;
+  static constexpr int kFixed =
+      kEpiBytes + kScaleEntries * kScaleFloats * 4 + kNumBarsMax * 8 + 16 + 1024;
   static constexpr int kStagesFit = (kSmemLimit - kFixed) / (kABytes + kBBytes);
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static_assert(kStages >= 2, "shared memory");
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + kStages * kABytes;
-  static constexpr int kOffScale = kOffB + kStages * kBBytes;
+  static constexpr int kOffEpi = kOffB + kStages * kBBytes;  // 1024-aligned (128-byte swizzle)
+  static_assert(kOffEpi % 1024 == 0, "staging alignment");
+  static constexpr int kOffScale = kOffEpi + kEpiBytes;
   static constexpr int kOffBar = kOffScale + kScaleEntries * kScaleFloats * 4;
   static constexpr int kNumBars = 2 * kStages + 2 * kTBuf + 2 * kScaleSlots + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -460,7 +467,8 @@ enum : int { kOutF32 = 0, kOutBf16 = 1, kOutE4m3 = 2 };
 template <int BN, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
 __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                const __grid_constant__ CUtensorMap tmap_b, const Params p) {
+                const __grid_constant__ CUtensorMap tmap_b,
+                const __grid_constant__ CUtensorMap tmap_c, const Params p) {
   using L = Cfg<BN, PAIR, PW>;
   constexpr int CM = L::CM;
   constexpr int kPromoWarps = L::kPromoWarps;
@@ -925,6 +933,48 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       }
 
       // ---- epilogue: registers -> global (bf16 RNE or fp32)
+      constexpr bool kTmaOut =
+          L::kEpiTma && (OUT == kOutF32 || (OUT == kOutBf16 && kCols % 64 == 0));
+      if constexpr (kTmaOut) {
+        // Through the warp's 4 KB staging tile (its 32 rows x 128 bytes, in
+        // the 128-byte-swizzled layout of the tensor map: 16-byte chunk c of
+        // row r at chunk c ^ (r % 8), so each quarter warp's writes hit
+        // distinct banks) and one tensor store per chunk of columns; the
+        // store clips rows and columns outside C.  The warp goes on to the
+        // next unit while the stores drain.
+        constexpr int kChunk = OUT == kOutF32 ? 32 : 64;  // columns per 128 bytes
+        uint8_t* ebuf = smem + L::kOffEpi + w * 4096;
+#pragma unroll
+        for (int j0 = 0; j0 < kCols; j0 += kChunk) {
+          if (lane == 0) ptx::bulk_wait_read_all();  // the last store has read the tile
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 v;
+            if constexpr (OUT == kOutF32) {
+              const int j = j0 + 4 * c;
+              v = make_uint4(__float_as_uint(acc[j]), __float_as_uint(acc[j + 1]),
+                             __float_as_uint(acc[j + 2]), __float_as_uint(acc[j + 3]));
+            } else {
+              const int j = j0 + 8 * c;
+              __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[j], acc[j + 1]);
+              __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
+              __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
+              v = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                             *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+            }
+            *reinterpret_cast<uint4*>(ebuf + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmap_c, ebuf, n0 + col0 + j0, m0 + lg * 32);
+            ptx::bulk_commit();
+          }
+        }
+        continue;
+      }
       const int m = m0 + row;
       if (m < p.M) {
         if constexpr (OUT == kOutE4m3) {
@@ -988,6 +1038,8 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         }
       }
     }
+    // this warp's output tensor stores have completed before the CTA exits
+    if (lane == 0) ptx::bulk_wait_all();
   }
 
   // ---- teardown: all roles done (or aborted); free TMEM
@@ -1121,8 +1173,14 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   }
   if (ws_need > g.ws_bytes) return cudaErrorInvalidValue;
 
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc = {};
   if (!make_tmap(&ta, g.a, g.M, g.K, kBM) || !make_tmap(&tb, g.b, g.N, g.K, L::kBH))
+    return cudaErrorInvalidValue;
+  // C for the tensor-store epilogue: 32 rows x 128 bytes per box
+  if (L::kEpiTma && OUT == kOutF32 && !make_tmap_2d(&tc, g.c, 4, g.M, g.N, 32, 32, true))
+    return cudaErrorInvalidValue;
+  if (L::kEpiTma && OUT == kOutBf16 && L::kCols % 64 == 0 &&
+      !make_tmap_2d(&tc, g.c, 2, g.M, g.N, 64, 32, true))
     return cudaErrorInvalidValue;
   Params p;
   p.sa = g.sa;
@@ -1185,7 +1243,7 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, p);
+  e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
