@@ -259,8 +259,8 @@ struct Cfg {
   static constexpr int kScaleB = BN + 4;  // B scales per slot (tile: BN, block: <= 3)
   static constexpr int kScaleFloats = kBM + kScaleB;
   // Epilogue staging for tensor-store output: 4 KB per promotion warp (its
-  // 32 rows x 128 bytes), when the warp's columns are whole 32-column chunks.
-  static constexpr bool kEpiTma = kCols % 32 == 0;
+  // 32 rows x up to 128 bytes).
+  static constexpr bool kEpiTma = kCols % 16 == 0;
   static constexpr int kEpiBytes = kEpiTma ? PW * 4096 : 0;
   static constexpr int kNumBarsMax = 2 * 8 + 2 * 4 + 2 * kScaleSlots + 1;
   static constexpr int kFixed =
@@ -933,23 +933,27 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
       }
 
       // ---- epilogue: registers -> global (bf16 RNE or fp32)
-      constexpr bool kTmaOut =
-          L::kEpiTma && (OUT == kOutF32 || (OUT == kOutBf16 && kCols % 64 == 0));
+      constexpr bool kTmaOut = L::kEpiTma && OUT != kOutE4m3;
       if constexpr (kTmaOut) {
-        // Through the warp's 4 KB staging tile (its 32 rows x 128 bytes, in
-        // the 128-byte-swizzled layout of the tensor map: 16-byte chunk c of
-        // row r at chunk c ^ (r % 8), so each quarter warp's writes hit
-        // distinct banks) and one tensor store per chunk of columns; the
-        // store clips rows and columns outside C.  The warp goes on to the
-        // next unit while the stores drain.
-        constexpr int kChunk = OUT == kOutF32 ? 32 : 64;  // columns per 128 bytes
+        // Through the warp's 4 KB staging tile and one tensor store per
+        // chunk of columns; the store clips rows and columns outside C, and
+        // the warp goes on to the next unit while the stores drain.  Chunks
+        // of 128 bytes per row (32 FP32 or 64 BF16 columns) when the warp's
+        // columns are whole such chunks, staged in the 128-byte-swizzled
+        // layout of the tensor map (16-byte chunk c of row r at c ^ (r % 8),
+        // so each quarter warp's writes hit distinct banks); otherwise chunks
+        // of 16 columns, unswizzled rows of 64 or 32 bytes.
+        constexpr int kElt = OUT == kOutF32 ? 4 : 2;
+        constexpr bool kWide = kCols % (128 / kElt) == 0;
+        constexpr int kChunk = kWide ? 128 / kElt : 16;  // columns per store
+        constexpr int kRowBytes = kChunk * kElt;
         uint8_t* ebuf = smem + L::kOffEpi + w * 4096;
 #pragma unroll
         for (int j0 = 0; j0 < kCols; j0 += kChunk) {
           if (lane == 0) ptx::bulk_wait_read_all();  // the last store has read the tile
           __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < kRowBytes / 16; ++c) {
             uint4 v;
             if constexpr (OUT == kOutF32) {
               const int j = j0 + 4 * c;
@@ -964,7 +968,8 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
               v = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
                              *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
             }
-            *reinterpret_cast<uint4*>(ebuf + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+            const int pos = kWide ? (c ^ (lane & 7)) : c;
+            *reinterpret_cast<uint4*>(ebuf + lane * kRowBytes + (pos << 4)) = v;
           }
           ptx::fence_proxy_async_smem();
           __syncwarp();
@@ -975,9 +980,10 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
         }
         continue;
       }
-      const int m = m0 + row;
-      if (m < p.M) {
-        if constexpr (OUT == kOutE4m3) {
+      static_assert(kTmaOut || OUT == kOutE4m3, "FP32 and BF16 outputs use tensor stores");
+      if constexpr (OUT == kOutE4m3) {
+        const int m = m0 + row;
+        if (m < p.M) {
           // One 1x128 group of the output row per thread: the warp's
           // kCols = 128 columns start on a multiple of 128.  Same rule as the
           // activation quantizer on FP32 values: s = fl32(amax / 448), codes
@@ -1007,33 +1013,6 @@ __global__ void __launch_bounds__(32 * (kFirstPromoWarp + PW), 1)
               *reinterpret_cast<uint4*>(crow + j2) = o;
             }
             p.c_scales[(size_t)(n / 128) * p.M + m] = g.s;
-          }
-        } else if (OUT == kOutBf16) {
-          __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(p.c) + (size_t)m * p.N;
-#pragma unroll
-          for (int j = 0; j < kCols; j += 8) {
-            const int n = n0 + col0 + j;
-            if (n < p.N) {
-              uint4 o;
-              __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[j], acc[j + 1]);
-              __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[j + 2], acc[j + 3]);
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[j + 4], acc[j + 5]);
-              __nv_bfloat162 b3 = __floats2bfloat162_rn(acc[j + 6], acc[j + 7]);
-              o.x = *reinterpret_cast<uint32_t*>(&b0);
-              o.y = *reinterpret_cast<uint32_t*>(&b1);
-              o.z = *reinterpret_cast<uint32_t*>(&b2);
-              o.w = *reinterpret_cast<uint32_t*>(&b3);
-              *reinterpret_cast<uint4*>(crow + n) = o;
-            }
-          }
-        } else {
-          float* crow = static_cast<float*>(p.c) + (size_t)m * p.N;
-#pragma unroll
-          for (int j = 0; j < kCols; j += 4) {
-            const int n = n0 + col0 + j;
-            if (n < p.N)
-              *reinterpret_cast<float4*>(crow + n) =
-                  make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
           }
         }
       }
@@ -1176,12 +1155,15 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   CUtensorMap ta, tb, tc = {};
   if (!make_tmap(&ta, g.a, g.M, g.K, kBM) || !make_tmap(&tb, g.b, g.N, g.K, L::kBH))
     return cudaErrorInvalidValue;
-  // C for the tensor-store epilogue: 32 rows x 128 bytes per box
-  if (L::kEpiTma && OUT == kOutF32 && !make_tmap_2d(&tc, g.c, 4, g.M, g.N, 32, 32, true))
-    return cudaErrorInvalidValue;
-  if (L::kEpiTma && OUT == kOutBf16 && L::kCols % 64 == 0 &&
-      !make_tmap_2d(&tc, g.c, 2, g.M, g.N, 64, 32, true))
-    return cudaErrorInvalidValue;
+  // C for the tensor-store epilogue: 32 rows x 128 bytes per box (swizzled)
+  // when the warps' columns are whole 128-byte chunks, else 32 rows x 16
+  // columns (unswizzled)
+  if (L::kEpiTma && OUT != kOutE4m3) {
+    const int elt = OUT == kOutF32 ? 4 : 2;
+    const bool wide = L::kCols % (128 / elt) == 0;
+    if (!make_tmap_2d(&tc, g.c, elt, g.M, g.N, wide ? 128 / elt : 16, 32, wide))
+      return cudaErrorInvalidValue;
+  }
   Params p;
   p.sa = g.sa;
   p.sb = g.sb;
