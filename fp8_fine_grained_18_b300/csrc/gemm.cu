@@ -1298,7 +1298,13 @@ cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
     return launch_variant<256, true, 8, PROMOTE, OUT, B_TILE>(g, stream);
   } else {
     int shape = g.tile;
-    if (shape < 0) shape = choose_tile(g.M, g.N, num_sms_current_device());
+    if (shape < 0) {
+      shape = choose_tile(g.M, g.N, num_sms_current_device());
+      // the un-promoted variant runs at the tensor pipe's rate, where the
+      // pair's halved B reads from shared memory matter: the 256 x 256 pair
+      // in place of the one-CTA 128 x 256 tile (same waves)
+      if (!PROMOTE && shape == kTile128x256) shape = kTile256x256Pair;
+    }
     switch (shape) {
       case kTile256x192PairW12:
         return launch_variant<192, true, 12, PROMOTE, OUT, B_TILE>(g, stream);
