@@ -982,15 +982,25 @@ struct Q3S {
         dequant4(tw[r * 32 + cq], s_row, xv);
       }
     };
-    float mn[4] = {0.0f, 0.0f, 0.0f, 0.0f}, mc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // column maxima that propagate NaN; the NaN-free maxima equal them
+    // unless a column holds a NaN, and only then are they recounted
+    float mn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 4
     for (int i = 0; i < 16; ++i) {
       float xv[4];
       dq(i, srow[i], xv);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        mn[c] = fmax_abs_nan(mn[c], xv[c]);
-        mc[c] = fmaxf(mc[c], fabsf(xv[c]));
+      for (int c = 0; c < 4; ++c) mn[c] = fmax_abs_nan(mn[c], xv[c]);
+    }
+    float mc[4] = {mn[0], mn[1], mn[2], mn[3]};
+    if (mn[0] != mn[0] || mn[1] != mn[1] || mn[2] != mn[2] || mn[3] != mn[3]) {
+      mc[0] = mc[1] = mc[2] = mc[3] = 0.0f;
+#pragma unroll 1
+      for (int i = 0; i < 16; ++i) {
+        float xv[4];
+        dq(i, srow[i], xv);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mc[c] = fmaxf(mc[c], fabsf(xv[c]));
       }
     }
     float* red = reinterpret_cast<float*>(scr + kOffRed);  // [2][8][128]
