@@ -243,6 +243,18 @@ def _bf16_dev(torch, bits, dev):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
 
+def step_config(M, N, K, seed, world):
+    """The workload both arms report (the reference arm times a bounded
+    sample of it, described in its cpu_baseline)."""
+    return {"workload": "large-K accumulation stress Fprop: quantize A and B 1x128, "
+                        "block-scaled FP8 GEMM promoted every 128 K, FP32 out",
+            "M": M, "N": N, "K": K, "seed": seed,
+            "inputs": "A, B U(-1,1) rows x 10^U(-2,2), bf16",
+            "l2": "flushed between steps (256 MB write, outside the timed events); "
+                  "inputs 268 MB each, larger than L2",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -364,13 +376,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": "large-K accumulation stress Fprop: quantize A and B 1x128, "
-                               "block-scaled FP8 GEMM promoted every 128 K, FP32 out",
-                   "M": M, "N": N, "K": K, "seed": w.seed,
-                   "inputs": "A, B U(-1,1) rows x 10^U(-2,2), bf16",
-                   "l2": "flushed between steps (256 MB write, outside the timed events); "
-                         "inputs 268 MB each, larger than L2",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(M, N, K, w.seed, world),
         "roofline": roofline, "kernels": kernels, "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(), "wall_timed_s": round(wall, 4),
@@ -849,8 +855,7 @@ def run_reference(args):
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-           "config": {"workload": "large-K accumulation stress Fprop (CPU oracle sample)",
-                      "M": M, "N": N, "K": K, "seed": w.seed},
+           "config": step_config(M, N, K, w.seed, world),
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
                             "cores": oracle.num_threads(), "sample": sample},
            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
