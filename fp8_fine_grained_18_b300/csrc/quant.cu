@@ -899,18 +899,6 @@ struct Q1TS {
   }
 };
 
-// Four codes (one word) of one row, dequantized with that row's scale:
-// x_hat = decode(code) * s, one round-to-nearest multiply each.
-__device__ __forceinline__ void dequant4(uint32_t w, float s, float (&o)[4]) {
-  const float2 s2 = make_float2(s, s);
-  const float2 a = ptx::mul2_rn(e4m3x2_decode(w & 0xFFFFu), s2);
-  const float2 b = ptx::mul2_rn(e4m3x2_decode(w >> 16), s2);
-  o[0] = a.x;
-  o[1] = a.y;
-  o[2] = b.x;
-  o[3] = b.y;
-}
-
 // Four E5M6 codes (48 bits: lo word and the next 16 bits) of one row,
 // dequantized with that row's scale: one round-to-nearest multiply each.
 __device__ __forceinline__ void dequant4_e5m6(uint32_t lo, uint32_t hi16, float s,
@@ -930,20 +918,24 @@ __device__ __forceinline__ void dequant4_e5m6(uint32_t lo, uint32_t hi16, float 
 // Q3: 1x128 -> 128x1 re-tiling of cached codes.  A stage holds a tile of
 // 128 rows (one 128-token group) x 128 columns (one K-group) of codes and
 // its 128 row scales (E4M3 codes, or with E5 the packed 12-bit E5M6 cache).
-// Team thread (cq, part): columns 4 cq .. 4 cq + 3, rows 16 part ..
-// 16 part + 15.  The column maxima propagate NaN (max.NaN) and, separately,
-// ignore it, so a column that holds a NaN needs no extra pass.
+// Team thread (cq, part): columns 4 cq .. 4 cq + 3, rows kRows part ..
+// kRows part + kRows - 1 (two teams of 8 warps and 16 rows a thread for the
+// E5M6 cache; four teams of 4 warps and 32 rows for E4M3).  The column
+// maxima propagate NaN (max.NaN); only a column that holds a NaN has its
+// NaN-free maximum counted again.
 template <bool E5>
 struct Q3S {
   static constexpr int kRowBytes = E5 ? 192 : 128;
   static constexpr int kCodeBytes = 128 * kRowBytes;
   static constexpr int kStageBytes = kCodeBytes + 128 * 4;
-  static constexpr int kStages = E5 ? 4 : 6;
-  static constexpr int kTeams = 2;
+  static constexpr int kStages = E5 ? 4 : 8;
+  static constexpr int kTeams = E5 ? 2 : 4;
+  static constexpr int kTeamWarps = kConsumerWarps / kTeams;
+  static constexpr int kRows = 128 / kTeamWarps;  // rows of a tile per thread
   static constexpr bool kBulkStores = true;
   static constexpr int kOffScales = 128 * 128;
   static constexpr int kOffRed = kOffScales + 128 * 4;
-  static constexpr int kOffNr = kOffRed + 2 * 8 * 128 * 4;
+  static constexpr int kOffNr = kOffRed + 2 * kTeamWarps * 128 * 4;
   static constexpr int kScratchBytes = kOffNr + 128 * 4;
   static constexpr uint32_t kTx = kStageBytes;
   struct Params {
@@ -959,8 +951,174 @@ struct Q3S {
     ptx::bulk_load(dst + kCodeBytes, p.s + (int64_t)kb * p.M + (int64_t)mb * kGroup, 128 * 4,
                    bar);
   }
+  // Codes of every column slot j for 16 rows, four rows (4h .. 4h + 3) to a
+  // word, into staging row 4 cq + a[j], 16-byte chunk `chunk`.  pw holds the
+  // 16 rows' codes as row-pair words (rows16 below); sp[r2] the scales of
+  // rows 2 r2 and 2 r2 + 1.  kAllFast: every slot's group takes the
+  // reciprocal-based quotient (the per-slot test folds away).
+  template <bool kAllFast>
+  __device__ __forceinline__ static void code_pass(const uint32_t (&pw)[16], const float2 (&sp)[8],
+                                                   const GroupScale (&g)[4], const uint32_t (&a)[4],
+                                                   uint8_t* scr, int cq, int chunk) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      GroupScale gj = g[j];
+      if (kAllFast) gj.fast = true;
+      uint32_t o[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t wa = pw[4 * h + (j >> 1)], wb = pw[4 * h + 2 + (j >> 1)];
+        const float2 xa = ptx::mul2_rn(e4m3x2_decode((j & 1) ? wa >> 16 : wa), sp[2 * h]);
+        const float2 xb = ptx::mul2_rn(e4m3x2_decode((j & 1) ? wb >> 16 : wb), sp[2 * h + 1]);
+        o[h] = codes_f32x4(xa.x, xa.y, xb.x, xb.y, gj);
+      }
+      stage_chunk(scr, 4 * cq + a[j], chunk, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+
+  // 16 rows' codes from the stage as row-pair words: pw[2 r2] holds slots
+  // 0, 1 and pw[2 r2 + 1] slots 2, 3 of rows 2 r2, 2 r2 + 1 (tw and s4p
+  // point at the first row's word and scales).
+  __device__ __forceinline__ static void rows16(const uint32_t* tw, const float4* s4p,
+                                                uint32_t sel01, uint32_t sel23, uint32_t (&pw)[16],
+                                                float2 (&sp)[8]) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float4 s4 = s4p[h];
+      sp[2 * h] = make_float2(s4.x, s4.y);
+      sp[2 * h + 1] = make_float2(s4.z, s4.w);
+    }
+#pragma unroll
+    for (int r2 = 0; r2 < 8; ++r2) {
+      const uint32_t w0 = tw[(2 * r2) * 32], w1 = tw[(2 * r2 + 1) * 32];
+      pw[2 * r2] = __byte_perm(w0, w1, sel01);
+      pw[2 * r2 + 1] = __byte_perm(w0, w1, sel23);
+    }
+  }
+
+  // E4M3 cache.  A byte permute gathers the codes of two consecutive rows
+  // in one column into one 16-bit pair, so that every packed FP32 pair
+  // (dequantization, quotient, encoding) holds rows (i, i + 1) of one
+  // column: the row scales pair up straight from the stage, and the two
+  // codes come out adjacent in the transposed output.  Column slot j of a
+  // lane holds its column (j + rot) % 4 (rot = (cq / 2) % 4), which spreads
+  // each warp's staging writes over all banks.  Teams of four warps (one
+  // per SM sub-partition) take 32 rows a thread, read in blocks of 16 rows,
+  // once for the column maxima and again for the codes.
+  __device__ static void consume_e4m3(const uint8_t* stage, int tile, const Params& p,
+                                      const Team& tm) {
+    const int kb = tile % p.KB, mb = tile / p.KB;
+    const int64_t k0 = (int64_t)kb * kGroup, m0 = (int64_t)mb * kGroup;
+    const int cq = tm.tid & 31, part = tm.tid >> 5;
+    const uint32_t rot = (cq >> 1) & 3;
+    const uint32_t a[4] = {rot, (rot + 1) & 3, (rot + 2) & 3, (rot + 3) & 3};
+    // __byte_perm(w_i, w_i+1, sel): bytes (w_i[a], w_i+1[a], w_i[a'], w_i+1[a'])
+    const uint32_t sel01 = a[0] | ((a[0] + 4) << 4) | (a[1] << 8) | ((a[1] + 4) << 12);
+    const uint32_t sel23 = a[2] | ((a[2] + 4) << 4) | (a[3] << 8) | ((a[3] + 4) << 12);
+    const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage) + part * kRows * 32 + cq;
+    const float4* s4p = reinterpret_cast<const float4*>(stage + kCodeBytes) + part * (kRows / 4);
+    float mn[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // per slot, NaN-propagating
+#pragma unroll
+    for (int b = 0; b < kRows / 16; ++b) {
+      uint32_t pw[16];
+      float2 sp[8];
+      rows16(tw + b * 16 * 32, s4p + b * 4, sel01, sel23, pw, sp);
+#pragma unroll
+      for (int r2 = 0; r2 < 8; ++r2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w = pw[2 * r2 + (j >> 1)];
+          const float2 x = ptx::mul2_rn(e4m3x2_decode((j & 1) ? w >> 16 : w), sp[r2]);
+          mn[j] = fmax_abs_nan(fmax_abs_nan(mn[j], x.x), x.y);
+        }
+      }
+    }
+    float mc[4] = {mn[0], mn[1], mn[2], mn[3]};
+    if (mn[0] != mn[0] || mn[1] != mn[1] || mn[2] != mn[2] || mn[3] != mn[3]) {
+      mc[0] = mc[1] = mc[2] = mc[3] = 0.0f;
+#pragma unroll 1
+      for (int b = 0; b < kRows / 16; ++b) {
+        uint32_t pw[16];
+        float2 sp[8];
+        rows16(tw + b * 16 * 32, s4p + b * 4, sel01, sel23, pw, sp);
+#pragma unroll
+        for (int r2 = 0; r2 < 8; ++r2) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w = pw[2 * r2 + (j >> 1)];
+            const float2 x = ptx::mul2_rn(e4m3x2_decode((j & 1) ? w >> 16 : w), sp[r2]);
+            mc[j] = fmaxf(mc[j], fmaxf(fabsf(x.x), fabsf(x.y)));
+          }
+        }
+      }
+    }
+    uint8_t* scr = tm.scratch;
+    float* red = reinterpret_cast<float*>(scr + kOffRed);  // [2][kTeamWarps][128]
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      red[part * 128 + 4 * cq + a[j]] = mn[j];
+      red[kTeamWarps * 128 + part * 128 + 4 * cq + a[j]] = mc[j];
+    }
+    team_stage_wait(tm);
+    ptx::named_barrier(tm.bar, tm.threads);
+    float* sc = reinterpret_cast<float*>(scr + kOffScales);
+    float* nr = reinterpret_cast<float*>(scr + kOffNr);
+    column_scales(red, sc, nr, part, cq);
+    ptx::named_barrier(tm.bar, tm.threads);
+    GroupScale g[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      g[j].s = sc[4 * cq + a[j]];
+      g[j].nr = nr[4 * cq + a[j]];
+      g[j].fast = g[j].nr != 0.0f;
+    }
+    const bool all_fast = g[0].fast && g[1].fast && g[2].fast && g[3].fast;
+#pragma unroll 1
+    for (int b = 0; b < kRows / 16; ++b) {
+      uint32_t pw[16];
+      float2 sp[8];
+      rows16(tw + b * 16 * 32, s4p + b * 4, sel01, sel23, pw, sp);
+      if (all_fast)
+        code_pass<true>(pw, sp, g, a, scr, cq, part * (kRows / 16) + b);
+      else
+        code_pass<false>(pw, sp, g, a, scr, cq, part * (kRows / 16) + b);
+    }
+    release_stage(tm.empty, tm.lane);
+    team_stage_store(tm, &p.map_out, scr, sc, (int)m0, (int)k0, p.sT + (int64_t)mb * p.K + k0);
+  }
+
+  // Each column's scale is made once: warp `part` finishes columns
+  // C part .. C part + C - 1 (C = 128 / kTeamWarps; with C = 16 lanes 16..31
+  // repeat lanes 0..15) from the team's partial maxima red[2][kTeamWarps][128],
+  // and writes s to the scales staging (which the previous tile's bulk store
+  // has read, see team_stage_wait) and -1/s (0 off the fast path) beside it.
+  __device__ static void column_scales(const float* red, float* sc, float* nr, int part, int cq) {
+    constexpr int C = 128 / kTeamWarps;
+    const int col = C * part + (cq % C);
+    float a = 0.0f, b = 0.0f;  // a is NaN if the column holds a NaN
+#pragma unroll
+    for (int q = 0; q < kTeamWarps; ++q) {
+      a = fmax_abs_nan(a, red[q * 128 + col]);
+      b = fmaxf(b, red[kTeamWarps * 128 + q * 128 + col]);
+    }
+    const GroupScale gc = make_scale(__float_as_uint(b), !(a < __uint_as_float(kF32Inf)), false);
+    if (cq < C) {
+      sc[col] = gc.s;
+      nr[col] = gc.fast ? gc.nr : 0.0f;
+    }
+  }
+
   __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
                                  const Team& tm) {
+    if constexpr (E5)
+      consume_e5m6(stage, tile, p, tm);
+    else
+      consume_e4m3(stage, tile, p, tm);
+  }
+
+  // E5M6 cache: 12-bit codes, four per 48 bits of a row.
+  __device__ static void consume_e5m6(const uint8_t* stage, int tile, const Params& p,
+                                      const Team& tm) {
     const int kb = tile % p.KB, mb = tile / p.KB;
     const int64_t k0 = (int64_t)kb * kGroup, m0 = (int64_t)mb * kGroup;
     const int t = tm.tid;
@@ -971,16 +1129,10 @@ struct Q3S {
     // the second pass): this keeps the kernel within the registers that 17
     // warps per SM leave (96 per thread).
     uint8_t* scr = tm.scratch;
-    const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage);
     const uint16_t* t16 = reinterpret_cast<const uint16_t*>(stage);
     auto dq = [&](int i, float s_row, float (&xv)[4]) {
-      const int r = part * 16 + i;
-      if constexpr (E5) {
-        const int h = r * 96 + 3 * cq;
-        dequant4_e5m6((uint32_t)t16[h] | ((uint32_t)t16[h + 1] << 16), t16[h + 2], s_row, xv);
-      } else {
-        dequant4(tw[r * 32 + cq], s_row, xv);
-      }
+      const int h = (part * 16 + i) * 96 + 3 * cq;
+      dequant4_e5m6((uint32_t)t16[h] | ((uint32_t)t16[h + 1] << 16), t16[h + 2], s_row, xv);
     };
     // column maxima that propagate NaN; the NaN-free maxima equal them
     // unless a column holds a NaN, and only then are they recounted
@@ -1004,31 +1156,15 @@ struct Q3S {
       }
     }
     float* red = reinterpret_cast<float*>(scr + kOffRed);  // [2][8][128]
+    static_assert(kTeamWarps == 8 && kRows == 16, "E5M6 re-tiling: teams of 8 warps");
     *reinterpret_cast<float4*>(red + part * 128 + 4 * cq) = make_float4(mn[0], mn[1], mn[2], mn[3]);
     *reinterpret_cast<float4*>(red + 1024 + part * 128 + 4 * cq) =
         make_float4(mc[0], mc[1], mc[2], mc[3]);
     team_stage_wait(tm);
     ptx::named_barrier(tm.bar, tm.threads);
-    // Each column's scale is made once: warp `part` finishes columns
-    // 16 part .. 16 part + 15 (lanes 16..31 repeat lanes 0..15) and writes s
-    // to the scales staging (which the previous tile's bulk store has read,
-    // see team_stage_wait) and -1/s (0 off the fast path) beside it.
     float* sc = reinterpret_cast<float*>(scr + kOffScales);
     float* nr = reinterpret_cast<float*>(scr + kOffNr);
-    {
-      const int col = 16 * part + (cq & 15);
-      float a = 0.0f, b = 0.0f;  // a is NaN if the column holds a NaN
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        a = fmax_abs_nan(a, red[q * 128 + col]);
-        b = fmaxf(b, red[1024 + q * 128 + col]);
-      }
-      const GroupScale gc = make_scale(__float_as_uint(b), !(a < __uint_as_float(kF32Inf)), false);
-      if (cq < 16) {
-        sc[col] = gc.s;
-        nr[col] = gc.fast ? gc.nr : 0.0f;
-      }
-    }
+    column_scales(red, sc, nr, part, cq);
     ptx::named_barrier(tm.bar, tm.threads);
     GroupScale g[4];
     {
