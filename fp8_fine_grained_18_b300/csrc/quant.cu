@@ -89,6 +89,15 @@ __device__ __forceinline__ uint2 codes_bf16x8(uint4 v, const GroupScale& g) {
   return make_uint2(codes_bf16x4(v.x, v.y, g), codes_bf16x4(v.z, v.w, g));
 }
 
+// codes_bf16x4 for a group known to take the fast path, with the packed
+// operands s2 = (s, s) and nr2 = (-1/s, -1/s) already formed.
+__device__ __forceinline__ uint32_t codes_bf16x4_fast(uint32_t wa, uint32_t wb, float2 s2,
+                                                      float2 nr2) {
+  const float2 qa = neg_quotient_1step_x2(make_float2(bf16_lo(wa), bf16_hi(wa)), s2, nr2);
+  const float2 qb = neg_quotient_1step_x2(make_float2(bf16_lo(wb), bf16_hi(wb)), s2, nr2);
+  return (e4m3x2(qa.x, qa.y) | (e4m3x2(qb.x, qb.y) << 16)) ^ 0x80808080u;
+}
+
 __device__ __forceinline__ GroupScale shfl_scale(const GroupScale& g, int src) {
   GroupScale o;
   o.s = __shfl_sync(kFull, g.s, src);
@@ -249,14 +258,33 @@ struct Q1 {
     const int64_t col = (int64_t)kb * kGroup + l16 * 8;
 #pragma unroll
     for (int b = 0; b < R / 4; ++b) {
+      // lane i (< 4) of the half-warp made row 4b + i's scale; -1/s is 0
+      // off the fast path, and one vote takes the warp's rows down it
       const GroupScale mine = make_scale(mj[b], pj[b] >= kBf16Inf, true);
+      const float nmine = mine.fast ? mine.nr : 0.0f;
+      if (__all_sync(kFull, l16 >= 4 || mine.fast)) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const GroupScale g = shfl_scale(mine, (lane & 16) + i);
-        const int64_t r = (int64_t)rt * kRows + hw + kHalfWarps * (4 * b + i);
-        if (r < p.M) {
-          *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[4 * b + i], g);
-          if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+        for (int i = 0; i < 4; ++i) {
+          const float si = __shfl_sync(kFull, mine.s, (lane & 16) + i);
+          const float ni = __shfl_sync(kFull, nmine, (lane & 16) + i);
+          const float2 s2 = make_float2(si, si), n2 = make_float2(ni, ni);
+          const int64_t r = (int64_t)rt * kRows + hw + kHalfWarps * (4 * b + i);
+          const uint4 x = v[4 * b + i];
+          if (r < p.M) {
+            *reinterpret_cast<uint2*>(p.q + r * p.K + col) =
+                make_uint2(codes_bf16x4_fast(x.x, x.y, s2, n2), codes_bf16x4_fast(x.z, x.w, s2, n2));
+            if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const GroupScale g = shfl_scale(mine, (lane & 16) + i);
+          const int64_t r = (int64_t)rt * kRows + hw + kHalfWarps * (4 * b + i);
+          if (r < p.M) {
+            *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[4 * b + i], g);
+            if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+          }
         }
       }
     }
@@ -756,7 +784,10 @@ struct Q1TS {
   static constexpr int kOffScales = 128 * 128;
   static constexpr int kOffRed = kOffScales + 128 * 4;
   static constexpr int kOffNr = kOffRed + 2 * 4 * 64 * 4;
-  static constexpr int kScratchBytes = kOffNr + 128 * 4;
+  // DUAL: per tile row (s, s, -1/s, -1/s) of its 1x128 group (-1/s = 0 off
+  // the fast path), from the lanes that made the scale to the whole half-warp
+  static constexpr int kOffRowS = kOffNr + 128 * 4;
+  static constexpr int kScratchBytes = kOffRowS + (DUAL ? 128 * 16 : 0);
   static constexpr uint32_t kTx = kStageBytes;
   struct Params {
     CUtensorMap map_out;  // qT [K][M] bytes, 128 x 128 box, 128-byte swizzle (64-byte aligned)
@@ -779,44 +810,52 @@ struct Q1TS {
     const int hw = t >> 4, l16 = t & 15;
     if constexpr (DUAL) {
       // 1x128 tiles first (their registers are free again before the 128x1
-      // pass): half-warp hw owns rows hw, hw + 16, ..., hw + 112; lane l16
-      // holds 8 consecutive elements of each, lanes 0..7 compute the eight
-      // rows' scales.
+      // pass): half-warp hw owns rows hw + 16 i (i < 8), lane l16 holds 8
+      // consecutive elements of each.  The row maxima reduce two rows to a
+      // shuffle (q1_row_max, rows 4b .. 4b + 3 to lanes 0..3); those lanes
+      // make the scales and leave them, with the packed quotient operands,
+      // in a per-row table that the half-warp reads back.
       uint4 v[8];
       const uint4* st = reinterpret_cast<const uint4*>(stage);
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = st[(hw + 16 * i) * 16 + l16];
-      // lane j (of 0..7) of the half-warp keeps row j's maxima
-      uint32_t mj = 0, pj = 0;
-      bool nan_seen = false;
+      uint32_t mj[2], pj[2];
+      q1_row_max(v, l16, mj[0], pj[0]);
+      q1_row_max(v + 4, l16, mj[1], pj[1]);
+      float4* rs = reinterpret_cast<float4*>(tm.scratch + kOffRowS);
+      bool fast = true;
+      if (l16 < 4) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t mm = halves_max(mag_pair_max(
-            mag_pair_max(mag_pair_max(mag_pair_max(0u, v[i].x), v[i].y), v[i].z), v[i].w));
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
-        if ((l16 & 7) == i) pj = mj = mm;
-        nan_seen |= mm > kBf16Inf;
-      }
-      if (__any_sync(kFull, nan_seen)) {  // rare: recount without NaN
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint32_t mm = halves_max(mag_pair_max_no_nan(
-              mag_pair_max_no_nan(mag_pair_max_no_nan(mag_pair_max_no_nan(0u, v[i].x), v[i].y),
-                                  v[i].z),
-              v[i].w));
-#pragma unroll
-          for (int off = 8; off >= 1; off >>= 1) mm = max(mm, __shfl_xor_sync(kFull, mm, off));
-          if ((l16 & 7) == i) mj = mm;
+        for (int b = 0; b < 2; ++b) {
+          const GroupScale g = make_scale(mj[b], pj[b] >= kBf16Inf, true);
+          const float n = g.fast ? g.nr : 0.0f;
+          const int r = hw + 16 * (4 * b + l16);
+          rs[r] = make_float4(g.s, g.s, n, n);
+          p.s[(int64_t)kb * p.M + m0 + r] = g.s;
+          fast = fast && g.fast;
         }
       }
-      const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
+      __syncwarp();
+      uint8_t* qrow = p.q + (m0 + hw) * p.K + k0 + l16 * 8;
+      if (__all_sync(kFull, fast)) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const GroupScale g = shfl_scale(mine, (tm.lane & 16) + i);
-        const int64_t r = m0 + hw + 16 * i;
-        *reinterpret_cast<uint2*>(p.q + r * p.K + k0 + l16 * 8) = codes_bf16x8(v[i], g);
-        if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+        for (int i = 0; i < 8; ++i) {
+          const float4 c = rs[hw + 16 * i];
+          const float2 s2 = make_float2(c.x, c.y), n2 = make_float2(c.z, c.w);
+          *reinterpret_cast<uint2*>(qrow + (int64_t)16 * i * p.K) =
+              make_uint2(codes_bf16x4_fast(v[i].x, v[i].y, s2, n2),
+                         codes_bf16x4_fast(v[i].z, v[i].w, s2, n2));
+        }
+      } else {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+          GroupScale g;
+          g.s = rs[hw + 16 * i].x;
+          g.nr = rs[hw + 16 * i].z;
+          g.fast = g.nr != 0.0f;
+          *reinterpret_cast<uint2*>(qrow + (int64_t)16 * i * p.K) =
+              codes_bf16x8(st[(hw + 16 * i) * 16 + l16], g);
+        }
       }
     }
     uint32_t w[32];
@@ -861,39 +900,44 @@ struct Q1TS {
       }
     }
     ptx::named_barrier(tm.bar, tm.threads);
-    GroupScale glo, ghi;
-    {
-      const float2 s2 = *reinterpret_cast<const float2*>(sc + 2 * cp);
-      const float2 n2 = *reinterpret_cast<const float2*>(nr + 2 * cp);
-      glo.s = s2.x;
-      glo.nr = n2.x;
-      glo.fast = n2.x != 0.0f;
-      ghi.s = s2.y;
-      ghi.nr = n2.y;
-      ghi.fast = n2.y != 0.0f;
-    }
-    uint32_t olo[8], ohi[8];
+    // The thread's two columns in the order it stages them: lanes with
+    // (cp / 4) odd take the odd column first, which spreads each warp's
+    // staging writes over all banks.
+    const uint32_t hi_first = (cp >> 2) & 1;
+    const uint32_t sel_a = hi_first ? 0x7632u : 0x5410u, sel_b = hi_first ? 0x5410u : 0x7632u;
+    const int ka = 2 * cp + (int)hi_first, kb2 = 2 * cp + 1 - (int)hi_first;
+    GroupScale ga, gb;
+    ga.s = sc[ka];
+    ga.nr = nr[ka];
+    ga.fast = ga.nr != 0.0f;
+    gb.s = sc[kb2];
+    gb.nr = nr[kb2];
+    gb.fast = gb.nr != 0.0f;
+    uint32_t oa[8], ob[8];
+    if (ga.fast && gb.fast) {
+      const float2 sa2 = make_float2(ga.s, ga.s), na2 = make_float2(ga.nr, ga.nr);
+      const float2 sb2 = make_float2(gb.s, gb.s), nb2 = make_float2(gb.nr, gb.nr);
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      // rows i .. i + 3 of each column
-      olo[i >> 2] = codes_bf16x4(__byte_perm(w[i], w[i + 1], 0x5410),
-                                 __byte_perm(w[i + 2], w[i + 3], 0x5410), glo);
-      ohi[i >> 2] = codes_bf16x4(__byte_perm(w[i], w[i + 1], 0x7632),
-                                 __byte_perm(w[i + 2], w[i + 3], 0x7632), ghi);
-    }
-    // output rows 2 cp (lo) and 2 cp + 1 (hi), chunks 2 part and 2 part + 1;
-    // lanes with (cp / 4) odd write hi first
-    const bool hi_first = (cp >> 2) & 1;
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const bool sel_hi = (c == 0) == hi_first;
-      const int k = 2 * cp + (sel_hi ? 1 : 0);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 d = sel_hi ? make_uint4(ohi[4 * h], ohi[4 * h + 1], ohi[4 * h + 2], ohi[4 * h + 3])
-                               : make_uint4(olo[4 * h], olo[4 * h + 1], olo[4 * h + 2], olo[4 * h + 3]);
-        stage_chunk(scr, k, 2 * part + h, d);
+      for (int i = 0; i < 32; i += 4) {  // rows i .. i + 3 of each column
+        oa[i >> 2] = codes_bf16x4_fast(__byte_perm(w[i], w[i + 1], sel_a),
+                                       __byte_perm(w[i + 2], w[i + 3], sel_a), sa2, na2);
+        ob[i >> 2] = codes_bf16x4_fast(__byte_perm(w[i], w[i + 1], sel_b),
+                                       __byte_perm(w[i + 2], w[i + 3], sel_b), sb2, nb2);
       }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        oa[i >> 2] = codes_bf16x4(__byte_perm(w[i], w[i + 1], sel_a),
+                                  __byte_perm(w[i + 2], w[i + 3], sel_a), ga);
+        ob[i >> 2] = codes_bf16x4(__byte_perm(w[i], w[i + 1], sel_b),
+                                  __byte_perm(w[i + 2], w[i + 3], sel_b), gb);
+      }
+    }
+    // output rows ka and kb2, chunks 2 part and 2 part + 1
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      stage_chunk(scr, ka, 2 * part + h, make_uint4(oa[4 * h], oa[4 * h + 1], oa[4 * h + 2], oa[4 * h + 3]));
+      stage_chunk(scr, kb2, 2 * part + h, make_uint4(ob[4 * h], ob[4 * h + 1], ob[4 * h + 2], ob[4 * h + 3]));
     }
     team_stage_store(tm, &p.map_out, scr, sc, (int)m0, (int)k0, p.sT + (int64_t)mb * p.K + k0);
   }
