@@ -66,13 +66,11 @@ __device__ __forceinline__ float group_scale(float amax, float fmt_max = kE4M3Ma
 // |x/s| >= 2^-12 (checked exhaustively over bf16 inputs against IEEE
 // division); below that every candidate codes as a zero of x's sign.
 // Two packed FP32 lanes are processed per instruction.
-__device__ __forceinline__ float2 neg_quotient_1step_x2(float2 x, float2 s2, float2 nr2) {
+__device__ __forceinline__ float2 neg_quotient_1step_x2(float2 x, float s, float nr) {
+  const float2 nr2 = make_float2(nr, nr), s2 = make_float2(s, s);
   const float2 q0 = ptx::mul2_rn(x, nr2);
   const float2 e = ptx::fma2_rn(q0, s2, x);
   return ptx::fma2_rn(e, nr2, q0);
-}
-__device__ __forceinline__ float2 neg_quotient_1step_x2(float2 x, float s, float nr) {
-  return neg_quotient_1step_x2(x, make_float2(s, s), make_float2(nr, nr));
 }
 
 // Two correction steps: the first makes the quotient faithful for any FP32

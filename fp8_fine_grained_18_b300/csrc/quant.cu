@@ -90,11 +90,16 @@ __device__ __forceinline__ uint2 codes_bf16x8(uint4 v, const GroupScale& g) {
 }
 
 // codes_bf16x4 for a group known to take the fast path, with the packed
-// operands s2 = (s, s) and nr2 = (-1/s, -1/s) already formed.
+// operands s2 = (s, s) and nr2 = (-1/s, -1/s) already formed: the same
+// one-step quotient as neg_quotient_1step_x2.
 __device__ __forceinline__ uint32_t codes_bf16x4_fast(uint32_t wa, uint32_t wb, float2 s2,
                                                       float2 nr2) {
-  const float2 qa = neg_quotient_1step_x2(make_float2(bf16_lo(wa), bf16_hi(wa)), s2, nr2);
-  const float2 qb = neg_quotient_1step_x2(make_float2(bf16_lo(wb), bf16_hi(wb)), s2, nr2);
+  auto quot = [&](float2 x) {
+    const float2 q0 = ptx::mul2_rn(x, nr2);
+    return ptx::fma2_rn(ptx::fma2_rn(q0, s2, x), nr2, q0);
+  };
+  const float2 qa = quot(make_float2(bf16_lo(wa), bf16_hi(wa)));
+  const float2 qb = quot(make_float2(bf16_lo(wb), bf16_hi(wb)));
   return (e4m3x2(qa.x, qa.y) | (e4m3x2(qb.x, qb.y) << 16)) ^ 0x80808080u;
 }
 
