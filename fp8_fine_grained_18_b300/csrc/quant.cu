@@ -948,16 +948,30 @@ struct Q1TS {
   }
 };
 
+// Two f16 (low half first) -> two exact floats.
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
+  float lo, hi;
+  asm("{.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;}"
+      : "=f"(lo), "=f"(hi) : "r"(h2));
+  return make_float2(lo, hi);
+}
+
 // Four E5M6 codes (48 bits: lo word and the next 16 bits) of one row,
 // dequantized with that row's scale: one round-to-nearest multiply each.
+// An E5M6 code is an IEEE half with its mantissa cut from 10 bits to 6
+// (same sign, 5-bit exponent with bias 15, subnormals, Inf and NaN), so a
+// code shifted left by 4 is the half of the same value: two codes go into
+// one f16x2 word by shifts and masks, and the half -> float conversion is
+// exact.
 __device__ __forceinline__ void dequant4_e5m6(uint32_t lo, uint32_t hi16, float s,
                                               float (&o)[4]) {
-  const uint64_t w = (uint64_t)lo | ((uint64_t)hi16 << 32);
+  // codes 0, 1 at bits 0..11 and 12..23 of lo; codes 2, 3 at bits 24..35
+  // and 36..47 of the 48-bit value {hi16:lo}
+  const uint32_t h01 = ((lo << 4) & 0x0000FFF0u) | ((lo << 8) & 0xFFF00000u);
+  const uint32_t h23 = (__funnelshift_r(lo, hi16, 20) & 0x0000FFF0u) | ((hi16 << 16) & 0xFFF00000u);
   const float2 s2 = make_float2(s, s);
-  const float2 a = ptx::mul2_rn(make_float2(e5m6_decode((uint32_t)w & 0xFFFu),
-                                            e5m6_decode((uint32_t)(w >> 12) & 0xFFFu)), s2);
-  const float2 b = ptx::mul2_rn(make_float2(e5m6_decode((uint32_t)(w >> 24) & 0xFFFu),
-                                            e5m6_decode((uint32_t)(w >> 36) & 0xFFFu)), s2);
+  const float2 a = ptx::mul2_rn(f16x2_to_f32x2(h01), s2);
+  const float2 b = ptx::mul2_rn(f16x2_to_f32x2(h23), s2);
   o[0] = a.x;
   o[1] = a.y;
   o[2] = b.x;
