@@ -53,7 +53,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`),
 # valid only for the kernel code it was taken on (a fingerprint of gemm.cu,
 # ptx.cuh and fp8_common.cuh without comments); null once the code changed.
-TRAFFIC = {"gemm": {"bytes": 1150966528 + 253376512, "src_sha": "832b0c20a049ff11"}}
+TRAFFIC = {"gemm": {"bytes": 1151670016 + 253349376, "src_sha": "4a84ad3cfe2738dc"}}
 
 
 def kernel_source_sha():
