@@ -3,10 +3,12 @@
 
 One step = one pass of the path over one batch of the large-K stress
 workload (M = N = 8192, K = 16384; both operands U(-1, 1) with per-row
-magnitudes 10^U(-2, 2), bf16 in, FP32 out): quantize A and B in 1x128 tiles
-(two launches), then the block-scaled FP8 GEMM with FP32 promotion every
-128 K (B scales per 1x128 tile of each B row).  This is the largest of the
-workloads, the one the throughput targets are set on.  With `--rows 1` (the
+magnitudes 10^U(-2, 2), bf16 in, FP32 out), as a forward GEMM: quantize A
+in 1x128 tiles and B in 128x128 blocks (two launches), then the
+block-scaled FP8 GEMM with FP32 promotion every 128 K.  This is the largest
+of the workloads, the one the throughput targets are set on.  (The same
+shape with B in 1x128 tiles, as the weight-gradient GEMM takes its B, is
+one of the rows.)  With `--rows 1` (the
 default) every other hot-path operation is also timed at its own workload
 shape and at the 8192 x 16384 bandwidth shape, and reported under `rows`,
 each with the SM clock sampled while it ran.
@@ -53,7 +55,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`),
 # valid only for the kernel code it was taken on (a fingerprint of gemm.cu,
 # ptx.cuh and fp8_common.cuh without comments); null once the code changed.
-TRAFFIC = {"gemm": {"bytes": 1151670016 + 253349376, "src_sha": "4a84ad3cfe2738dc"}}
+TRAFFIC = {"gemm": {"bytes": 1119746048 + 252459520, "src_sha": "4a84ad3cfe2738dc"}}
 
 
 def kernel_source_sha():
@@ -246,8 +248,8 @@ def _bf16_dev(torch, bits, dev):
 def step_config(M, N, K, seed, world):
     """The workload both arms report (the reference arm times a bounded
     sample of it, described in its cpu_baseline)."""
-    return {"workload": "large-K accumulation stress Fprop: quantize A and B 1x128, "
-                        "block-scaled FP8 GEMM promoted every 128 K, FP32 out",
+    return {"workload": "large-K accumulation stress Fprop: quantize A 1x128 and B 128x128 "
+                        "(two launches), block-scaled FP8 GEMM promoted every 128 K, FP32 out",
             "M": M, "N": N, "K": K, "seed": seed,
             "inputs": "A, B U(-1,1) rows x 10^U(-2,2), bf16",
             "l2": "flushed between steps (256 MB write, outside the timed events); "
@@ -285,18 +287,17 @@ def run_ours(args):
     qa = torch.empty((M, K), dtype=torch.uint8, device=dev)
     sa = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
     qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
-    sb = torch.empty((K // 128, N), dtype=torch.float32, device=dev)
+    sb = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
     c = torch.empty((M, N), dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 126 MB L2
     stream = torch.cuda.current_stream(dev)
-    tile = fp8bs.BSCALE_TILE_1x128
 
     def quantize():
         fp8bs.quant_act_1x128(a, q=qa, scales=sa)
-        fp8bs.quant_act_1x128(b, q=qb, scales=sb)
+        fp8bs.quant_weight_128x128(b, q=qb, scales=sb)
 
     def gemm():
-        fp8bs.gemm(qa, sa, qb, sb, tile, out_dtype=torch.float32, out=c)
+        fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_BLOCK_128x128, out_dtype=torch.float32, out=c)
 
     for _ in range(args.warmup):
         quantize()
@@ -343,7 +344,7 @@ def run_ours(args):
     if tr and tr.get("src_sha") == kernel_source_sha():
         traffic = tr["bytes"]
     roofline = {"bound": "tensor", "kernel": "gemm (block-scaled FP8, promoted every 128 K, "
-                                             "1x128 B scales, FP32 out)",
+                                             "128x128 B scales, FP32 out)",
                 "achieved": round(g_tflops, 2), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                 "frac": round(g_tflops / fp8_peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} bf16 burst {peaks['bf16_tflops']} x {FP8_OVER_BF16} "
@@ -351,9 +352,9 @@ def run_ours(args):
                 "frac_of_sustained": round(g_tflops / (peaks["bf16_tflops_sustained"] * FP8_OVER_BF16), 4),
                 "algorithmic_flops_per_launch": flops}
     hbm = peaks["hbm_gbs"]
-    q_gbs = 2 * algorithmic_bytes_q1(M, K) / (statistics.mean(t_q) * 1e-3) / 1e9
+    q_gbs = (algorithmic_bytes_q1(M, K) + algorithmic_bytes_q2(N, K)) / (statistics.mean(t_q) * 1e-3) / 1e9
     kernels = {
-        "quant_act_1x128 of A and of B (two launches)": {
+        "quant_act_1x128 of A, quant_weight_128x128 of B (two launches)": {
             "ms": round(statistics.mean(t_q), 4), "GB/s": round(q_gbs, 1),
             "frac_hbm": round(q_gbs / hbm, 4), "frac_hbm_nominal_8TBs": round(q_gbs / HBM_NOMINAL_GBS, 4)},
         "gemm": {"ms": round(g_ms, 4), "TFLOP/s": round(g_tflops, 1),
@@ -411,7 +412,7 @@ def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
             "qa": torch.empty((M, K), dtype=torch.uint8, device=dev),
             "sa": torch.empty((K // 128, M), dtype=torch.float32, device=dev),
             "qb": torch.empty((N, K), dtype=torch.uint8, device=dev),
-            "sb": torch.empty((K // 128, N), dtype=torch.float32, device=dev),
+            "sb": torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev),
             "c": torch.empty((M, N), dtype=torch.float32, device=dev),
             "c_pin": torch.empty((M, N), dtype=torch.float32).pin_memory(),
         })
@@ -440,8 +441,8 @@ def measure_e2e(fp8bs, torch, dev, a_host, b_host, M, N, K, steps):
                 if read[k] is not None:
                     comp.wait_event(read[k])  # step i-2's result has been read back
                 fp8bs.quant_act_1x128(st["a"], q=st["qa"], scales=st["sa"])
-                fp8bs.quant_act_1x128(st["b"], q=st["qb"], scales=st["sb"])
-                fp8bs.gemm(st["qa"], st["sa"], st["qb"], st["sb"], fp8bs.BSCALE_TILE_1x128,
+                fp8bs.quant_weight_128x128(st["b"], q=st["qb"], scales=st["sb"])
+                fp8bs.gemm(st["qa"], st["sa"], st["qb"], st["sb"], fp8bs.BSCALE_BLOCK_128x128,
                            out_dtype=torch.float32, out=st["c"])
                 done[k] = ev(); done[k].record(comp)
             with torch.cuda.stream(d2h):
@@ -678,6 +679,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
     qb, sb = fp8bs.quant_act_1x128(b)
     quant_row("Q1 8192x16384", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
               algorithmic_bytes_q1(Mb, Kb))
+    gemm_row("G1 stress 8192x8192x16384 f32 (1x128 B scales, as the weight gradient takes B)",
+             qa, sa, qb, sb, 1, torch.float32)
     gemm_row("G2 un-promoted stress 8192x8192x16384 f32", qa, sa, qb, sb, 1, torch.float32,
              promote=False)
     del b, qb, sb
@@ -714,7 +717,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
     return rows
 
 
-PROFILE_KERNELS = ("q1", "q1t", "dual", "q3", "q2", "q2t", "q1e5", "q3e5", "tensor", "gemm")
+PROFILE_KERNELS = ("q1", "q1t", "dual", "q3", "q2", "q2t", "q1e5", "q3e5", "tensor", "gemm",
+                   "gemm_tile")
 
 
 def profile_kernel(args):
@@ -733,12 +737,18 @@ def profile_kernel(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     n_el = M * K
     k = args.kernel
-    if k == "gemm":
+    if k in ("gemm", "gemm_tile"):
+        # gemm: the step's GEMM (B in 128x128 blocks); gemm_tile: B in 1x128 tiles
         b = torch.rand((M, K), generator=g, device=dev).mul_(2).sub_(1).to(torch.bfloat16)
         qa, sa = fp8bs.quant_act_1x128(a)
-        qb, sb = fp8bs.quant_act_1x128(b)
+        if k == "gemm":
+            qb, sb = fp8bs.quant_weight_128x128(b)
+            bkind = fp8bs.BSCALE_BLOCK_128x128
+        else:
+            qb, sb = fp8bs.quant_act_1x128(b)
+            bkind = fp8bs.BSCALE_TILE_1x128
         c = torch.empty((M, M), dtype=torch.float32, device=dev)
-        fn = lambda: fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_TILE_1x128, out_dtype=torch.float32, out=c)
+        fn = lambda: fp8bs.gemm(qa, sa, qb, sb, bkind, out_dtype=torch.float32, out=c)
         work, unit = 2.0 * M * M * K / 1e12, "TFLOP/s"
     else:
         qa, sa = fp8bs.quant_act_1x128(a)
@@ -791,19 +801,25 @@ def profile_kernel(args):
                       "rate": round(work / (ms * 1e-3), 1), "unit": unit}))
 
 
+def _b_rows(N, r0, n_s):
+    """First row of a sample of n_s rows of B: whole 128-row blocks, so that
+    the block quantizer sees the blocks the full-size quantization has."""
+    return ((r0 // 128) * 128) % (N - n_s + 1)
+
+
 def cpu_baseline(M, N, K, inp, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the step's workload:
-    quantize a few rows of A and of B (1x128) and compute their GEMM block
-    in double."""
+    quantize a few rows of A (1x128) and two 128-row blocks of B (128x128)
+    and compute their GEMM block in double."""
     import oracle
     oracle.lib()
     m_s, n_s = 8, 256
     t0 = time.perf_counter()
     qa, sa = oracle.quant_act_1x128(inp["A"][:m_s])
-    qb, sb = oracle.quant_act_1x128(inp["B"][:n_s])
+    qb, sb = oracle.quant_weight_128x128(inp["B"][:n_s])
     ms = np.repeat(np.arange(m_s), n_s)
     ns = np.tile(np.arange(n_s), m_s)
-    oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_TILE_1x128, ms, ns)
+    oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_BLOCK_128x128, ms, ns)
     secs = time.perf_counter() - t0
     # scale the sample to the budget: repeat while it is short
     reps = max(1, int(budget_s / max(secs, 1e-3) * 0.5))
@@ -811,16 +827,17 @@ def cpu_baseline(M, N, K, inp, budget_s=20.0):
     t0 = time.perf_counter()
     for r in range(reps):
         r0 = (r * m_s) % (M - m_s)
+        b0 = _b_rows(N, r0, n_s)
         qa, sa = oracle.quant_act_1x128(inp["A"][r0:r0 + m_s])
-        qb, sb = oracle.quant_act_1x128(inp["B"][r0:r0 + n_s])
-        oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_TILE_1x128, ms, ns)
+        qb, sb = oracle.quant_weight_128x128(inp["B"][b0:b0 + n_s])
+        oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_BLOCK_128x128, ms, ns)
     secs = time.perf_counter() - t0
     flops = 2.0 * m_s * n_s * K * reps
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s",
             "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{reps} repetitions of: quantize {m_s} rows of A and {n_s} rows of B "
-                      f"(1x128 tiles, K = {K}) and their {m_s}x{n_s}x{K} GEMM block in double "
-                      f"({secs:.1f} s of CPU time)"}
+            "sample": f"{reps} repetitions of: quantize {m_s} rows of A (1x128 tiles) and "
+                      f"{n_s} rows of B (128x128 blocks), K = {K}, and their {m_s}x{n_s}x{K} "
+                      f"GEMM block in double ({secs:.1f} s of CPU time)"}
 
 
 # ------------------------------------------------------- reference arm (CPU)
@@ -849,8 +866,8 @@ def run_reference(args):
         _ref_step(oracle, inp, (i * rows) % max(1, M - rows), rows, n_s, K)
     secs = time.perf_counter() - t0
     value = 2.0 * rows * n_s * K * args.steps / secs / 1e12
-    sample = (f"each step: {rows} rows of A and {n_s} rows of B quantized (1x128) and their "
-              f"{rows}x{n_s}x{K} GEMM block in double")
+    sample = (f"each step: {rows} rows of A (1x128 tiles) and {n_s} rows of B (128x128 "
+              f"blocks) quantized and their {rows}x{n_s}x{K} GEMM block in double")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
@@ -864,12 +881,12 @@ def run_reference(args):
 
 
 def _ref_step(oracle, inp, r0, rows, n_s, K):
+    b0 = _b_rows(inp["B"].shape[0], r0, n_s)
     qa, sa = oracle.quant_act_1x128(inp["A"][r0:r0 + rows])
-    qb, sb = oracle.quant_act_1x128(inp["B"][r0:r0 + n_s] if r0 + n_s <= inp["B"].shape[0]
-                                    else inp["B"][:n_s])
+    qb, sb = oracle.quant_weight_128x128(inp["B"][b0:b0 + n_s])
     ms = np.repeat(np.arange(rows), n_s)
     ns = np.tile(np.arange(n_s), rows)
-    return oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_TILE_1x128, ms, ns)
+    return oracle.gemm_sampled(qa, sa, qb, sb, oracle.BSCALE_BLOCK_128x128, ms, ns)
 
 
 def main():

@@ -223,6 +223,27 @@ def test_stress_full_sampled(fp8bs, oracle_mod):
     _check_sampled(fp8bs, oracle_mod, a, sa, b, sb, TILE, "stress", samples=1500, bf16=False)
 
 
+def test_bench_stress_step_full_sampled(fp8bs, oracle_mod):
+    """The benchmark's headline step as it launches it: A quantized in 1x128
+    tiles and B in 128x128 blocks on the device (two launches), then the
+    promoted GEMM with block B scales, the automatic tile and FP32 output at
+    8192 x 8192 x 16384; the device codes and scales equal the oracle's, and
+    sampled outputs match the oracle's double sums."""
+    inp = synth.make_inputs("stress")
+    qa, sa = fp8bs.quant_act_1x128(dev_bf16(inp["A"]))
+    qb, sb = fp8bs.quant_weight_128x128(dev_bf16(inp["B"]))
+    c = fp8bs.gemm(qa, sa, qb, sb, BLOCK, out_dtype=torch.float32)
+    a_ref, sa_ref = oracle_mod.quant_act_1x128(inp["A"])
+    b_ref, sb_ref = oracle_mod.quant_weight_128x128(inp["B"])
+    assert np.array_equal(host(qa), a_ref) and np.array_equal(host(sa).view(np.uint32), sa_ref.view(np.uint32))
+    assert np.array_equal(host(qb), b_ref) and np.array_equal(host(sb).view(np.uint32), sb_ref.view(np.uint32))
+    M, N = a_ref.shape[0], b_ref.shape[0]
+    ms, ns = _sample_positions(M, N, 1500, 11)
+    ref = oracle_mod.gemm_sampled(a_ref, sa_ref, b_ref, sb_ref, BLOCK, ms, ns)
+    v = host(c[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()])
+    assert_gemm_f32(v, ref, "bench stress step")
+
+
 def test_bench_step_full_sampled(fp8bs, oracle_mod):
     """The dense projection step exactly as the benchmark launches it: both
     operands quantized in one launch, then the GEMM with the automatic tile
