@@ -17,8 +17,9 @@ each with the SM clock sampled while it ran.
 
 Prints one JSON line.  `value` is whole-job TFLOP/s (2*M*N*K per step per
 GPU) with inputs resident in HBM, CUDA-event timed on the launching stream,
-L2 flushed between steps (the inputs, 268 MB each, are larger than L2
-anyway); `e2e` is the same metric through the C ABI from pinned host
+L2 flushed between steps (a 256 MB write and then a 256 MB read, so the
+written lines go back to DRAM outside the timed events; the inputs, 268 MB
+each, are larger than L2 anyway); `e2e` is the same metric through the C ABI from pinned host
 buffers (host<->device copies of both operands and of C inside the timed
 region).  Under torchrun every rank runs its own replica (weak scaling; no
 collective on the data path) and the slowest rank's time is used.
@@ -241,6 +242,22 @@ def algorithmic_bytes_q3(M, K):
     return M * K * 2 + 2 * 4 * M * (K // 128)
 
 
+class L2Flush:
+    """Run between timed launches, outside their events: write a 256 MB
+    buffer (twice the 126 MB L2), then read a second 256 MB buffer.  The read
+    evicts the written lines, so their write-back to DRAM happens here and
+    not inside the next timed kernel, which starts with an L2 holding only
+    clean, unrelated data."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros((256 << 20) // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
+
 def _bf16_dev(torch, bits, dev):
     return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
@@ -252,8 +269,8 @@ def step_config(M, N, K, seed, world):
                         "(two launches), block-scaled FP8 GEMM promoted every 128 K, FP32 out",
             "M": M, "N": N, "K": K, "seed": seed,
             "inputs": "A, B U(-1,1) rows x 10^U(-2,2), bf16",
-            "l2": "flushed between steps (256 MB write, outside the timed events); "
-                  "inputs 268 MB each, larger than L2",
+            "l2": "flushed between steps outside the timed events (a 256 MB write, then a "
+                  "256 MB read that evicts the written lines); inputs 268 MB each, larger than L2",
             "parallelism": f"replicas x{world}"}
 
 
@@ -289,7 +306,7 @@ def run_ours(args):
     qb = torch.empty((N, K), dtype=torch.uint8, device=dev)
     sb = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
     c = torch.empty((M, N), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > 126 MB L2
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
 
     def quantize():
@@ -314,7 +331,7 @@ def run_ours(args):
     wall0 = time.perf_counter()
     with sampler:
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             e = ev[i]
             e[0].record(stream)
             quantize()
@@ -483,7 +500,7 @@ def _time_ms(fn, torch, flush, min_ms=60.0, min_iters=10, max_iters=2000):
     def batch(n):
         evs = []
         for _ in range(n):
-            flush.zero_()
+            flush()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             fn()
@@ -513,7 +530,7 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
     contains it are timed (their inputs are still prepared)."""
     hbm = peaks["hbm_gbs"]
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     rows = {}
 
     def timed(fn):
@@ -734,7 +751,7 @@ def profile_kernel(args):
     g = torch.Generator(device=dev)
     g.manual_seed(4)
     a = torch.rand((M, K), generator=g, device=dev).mul_(2).sub_(1).to(torch.bfloat16)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     n_el = M * K
     k = args.kernel
     if k in ("gemm", "gemm_tile"):
@@ -784,12 +801,12 @@ def profile_kernel(args):
             fn, nb = (lambda: fp8bs.quant_per_tensor(a, q=qpt, scale=spt)), 3 * n_el + 4
         work, unit = nb / 1e9, "GB/s"
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         fn()
     torch.cuda.synchronize()
     times = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
