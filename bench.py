@@ -698,6 +698,20 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
               algorithmic_bytes_q1(Mb, Kb))
     gemm_row("G1 stress 8192x8192x16384 f32 (1x128 B scales, as the weight gradient takes B)",
              qa, sa, qb, sb, 1, torch.float32)
+    # the whole stress step with B in 1x128 tiles: Q1 of A and of B, then
+    # the GEMM with per-column B scales
+    name = "stress step 8192x8192x16384 with 1x128 B tiles: Q1 of A, Q1 of B, G1 f32"
+    if not skip(name):
+        cst = torch.empty((Mb, Mb), dtype=torch.float32, device=dev)
+
+        def tile_step():
+            fp8bs.quant_act_1x128(a, q=qa, scales=sa)
+            fp8bs.quant_act_1x128(b, q=qb, scales=sb)
+            fp8bs.gemm(qa, sa, qb, sb, fp8bs.BSCALE_TILE_1x128, out_dtype=torch.float32, out=cst)
+        ms, n, clk = timed(tile_step)
+        tf = 2.0 * Mb * Mb * Kb / (ms * 1e-3) / 1e12
+        rows[name] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1), "launches": n, "clocks": clk}
+        del cst
     gemm_row("G2 un-promoted stress 8192x8192x16384 f32", qa, sa, qb, sb, 1, torch.float32,
              promote=False)
     del b, qb, sb
