@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`),
 # valid only for the kernel code it was taken on (a fingerprint of gemm.cu,
 # ptx.cuh and fp8_common.cuh without comments); null once the code changed.
-TRAFFIC = {"gemm": {"bytes": 1119746048 + 252459520, "src_sha": "4a84ad3cfe2738dc"}}
+TRAFFIC = {"gemm": {"bytes": 1124593664 + 252510976, "src_sha": "8774b383017cc59a"}}
 
 
 def kernel_source_sha():
@@ -541,17 +541,27 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
     def skip(name):
         return only is not None and only not in name
 
-    def gemm_row(name, qa, sa, qb, sb, bkind, out_dtype, promote=True):
+    def gemm_row(name, qa, sa, qb, sb, bkind, out_dtype, promote=True, streamk=False):
         if skip(name):
             return
         M, K = qa.shape
         N = qb.shape[0]
         c = torch.empty((M, N), dtype=out_dtype, device=dev)
-        ms, n, clk = timed(lambda: fp8bs.gemm(qa, sa, qb, sb, bkind, out_dtype=out_dtype, out=c,
-                                              promote=promote))
+        extra = {}
+        if streamk:
+            need = fp8bs.gemm_streamk_workspace(M, N, K, bkind, out_dtype)
+            wsp = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+            fn = lambda: fp8bs.gemm_streamk(qa, sa, qb, sb, bkind, out_dtype=out_dtype,  # noqa: E731
+                                            workspace=wsp if need else None, out=c)
+            extra = {"workspace_bytes": need}
+        else:
+            fn = lambda: fp8bs.gemm(qa, sa, qb, sb, bkind, out_dtype=out_dtype, out=c,  # noqa: E731
+                                    promote=promote)
+        ms, n, clk = timed(fn)
         tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
         rows[name] = {"M": M, "N": N, "K": K, "ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                      "frac_fp8_peak": round(tf / fp8_peak, 4), "launches": n, "clocks": clk}
+                      "frac_fp8_peak": round(tf / fp8_peak, 4), "launches": n, "clocks": clk,
+                      **extra}
 
     def quant_row(name, fn, nbytes):
         if skip(name):
@@ -606,6 +616,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
               lambda: fp8bs.quant_act_and_weight(a, b, q=qa, scales=sa, qw=qb, w_scales=sb),
               algorithmic_bytes_q1(4096, 7168) + algorithmic_bytes_q2(7168, 7168))
     gemm_row("G1 dense 4096x7168x7168 bf16", qa, sa, qb, sb, 0, torch.bfloat16)
+    gemm_row("G1 dense 4096x7168x7168 bf16, stream-K call (uneven last wave spread)",
+             qa, sa, qb, sb, 0, torch.bfloat16, streamk=True)
     quant_row("Q1 dense A 4096x7168 (own launch)", lambda: fp8bs.quant_act_1x128(a, q=qa, scales=sa),
               algorithmic_bytes_q1(4096, 7168))
     quant_row("Q2 dense W 7168x7168 (own launch)",
@@ -665,6 +677,8 @@ def measure_rows(fp8bs, torch, dev, peaks, index, only=None):
               algorithmic_bytes_q2(7168, 2048, transposed=True))
     gemm_row("G1 dgrad 4096x2048x7168 bf16", qdy, sdy, qwT, swT, 0, torch.bfloat16)
     gemm_row("G1 wgrad 7168x2048x4096 f32 (1x128 B scales)", qdyT, sdyT, qxT, sxT, 1, torch.float32)
+    gemm_row("G1 wgrad 7168x2048x4096 f32 (1x128 B scales), stream-K call (uneven last wave spread)",
+             qdyT, sdyT, qxT, sxT, 1, torch.float32, streamk=True)
     # stream-K: a long-K problem with too few tiles for the SMs (the weight
     # gradient of a 512-wide layer over 16384 tokens: 4 pair tiles)
     name = "G1 stream-K 512x512x16384 f32 (1x128 B scales, 4 tiles split over every SM)"

@@ -1084,6 +1084,20 @@ struct KernelInfo {
   int max_ctas = 0;  // persistent grid size (a multiple of CM)
 };
 
+// Stream-K's cost in waves beyond the work itself, fitted to timings of
+// 128 x 256 tiles: split over every CTA, 448 tiles (3.03 waves) ran like
+// 3.56 waves and 896 tiles (6.05 waves) like 6.61.
+constexpr double kSkCostWaves = 0.55;
+
+// Whether spreading the last waves over every CTA group beats whole units:
+// the last wave of `units` whole units on `groups` groups leaves them idle
+// for more than stream-K's cost.
+inline bool sk_worth(int64_t units, int64_t groups) {
+  if (groups <= 0 || units <= 0) return false;
+  const int64_t waves = (units + groups - 1) / groups;
+  return (double)waves - (double)units / groups > kSkCostWaves;
+}
+
 template <int BN, bool PAIR, int PW, bool PROMOTE, int OUT, bool B_TILE>
 cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   using L = Cfg<BN, PAIR, PW>;
@@ -1133,13 +1147,14 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   }
   if (ki.err != cudaSuccess) return ki.err;
 
-  // Stream-K plan.  When whole units would keep the CTA groups busy less
-  // than 60% of the time (few units for the groups: e.g. 16 pair tiles on
-  // 74 pairs), the units of the last two waves (all of them, below two
-  // waves) have their K-groups spread evenly over every group.  Above that,
-  // the shares' hand-off through the workspace costs more than the idle
-  // groups (measured: 128 tiles on 74 pairs, 86% busy, ran 12% slower
-  // split).  Workspace:
+  // Stream-K plan.  When the last wave of whole units would leave the CTA
+  // groups idle for more than sk_worth's share of a wave (e.g. 16 pair
+  // tiles on 74 pairs, or 448 one-CTA tiles on 148 CTAs: 3.03 waves), the
+  // units of the last two waves (all of them, below two waves) have their
+  // K-groups spread evenly over every group.  Below that, the shares'
+  // hand-off through the workspace costs more than the idle groups
+  // (measured: 128 tiles on 74 pairs, 1.73 waves, ran 12% slower split).
+  // Workspace:
   // two FP32 shares of a CTA's 128 x BN accumulator per group (the partial
   // first and last segments of its share), then one arrival counter per
   // stream-K unit, CTA and promotion warp.
@@ -1149,10 +1164,9 @@ cudaError_t launch_variant(const GemmArgs& g, cudaStream_t stream) {
   int64_t sk_begin = all_units;
   size_t ws_shares = 0, ws_need = 0;
   if (PROMOTE && OUT != kOutE4m3 && (g.ws != nullptr || g.ws_need != nullptr) && groups > 0) {
-    const int64_t waves = (all_units + groups - 1) / groups;
     // (the stream-K iteration count must fit an int)
     const int64_t sk_units_max = all_units / groups >= 1 ? all_units % groups + groups : all_units;
-    if (10 * all_units < 6 * waves * groups && sk_units_max * (g.K / kBK) < (int64_t(1) << 31)) {
+    if (sk_worth(all_units, groups) && sk_units_max * (g.K / kBK) < (int64_t(1) << 31)) {
       sk_begin = all_units / groups >= 1 ? (all_units / groups - 1) * groups : 0;
       ws_shares = (size_t)2 * groups * CM * kBM * BN * sizeof(float);
       ws_need = ws_shares + (size_t)(all_units - sk_begin) * CM * PW * sizeof(unsigned int);
@@ -1261,7 +1275,7 @@ enum TileShape {
   kTile256x128PairW16 = 10,
 };
 
-TileShape choose_tile(int64_t M, int64_t N, int sms) {
+TileShape choose_tile(int64_t M, int64_t N, int sms, bool streamk) {
   struct Cand {
     TileShape s;
     int bm, bn;
@@ -1281,7 +1295,11 @@ TileShape choose_tile(int64_t M, int64_t N, int sms) {
     const int64_t units = ((M + c.bm - 1) / c.bm) * ((N + c.bn - 1) / c.bn);
     const int64_t slots = sms / (c.bm / kBM);
     const int64_t waves = (units + slots - 1) / slots;
-    const double cost = (double)waves * c.bn / c.eff;
+    // with stream-K (when the plan would split this shape) the work counts
+    // in fractional waves plus the hand-off's cost
+    const double w = streamk && sk_worth(units, slots) ? (double)units / slots + kSkCostWaves
+                                                       : (double)waves;
+    const double cost = w * c.bn / c.eff;
     if (cost < best_cost) {
       best_cost = cost;
       best = c.s;
@@ -1299,7 +1317,10 @@ cudaError_t launch_shape(const GemmArgs& g, cudaStream_t stream) {
   } else {
     int shape = g.tile;
     if (shape < 0) {
-      shape = choose_tile(g.M, g.N, num_sms_current_device());
+      // stream-K calls (a workspace given or asked for) weigh each shape
+      // with the stream-K plan it would get
+      shape = choose_tile(g.M, g.N, num_sms_current_device(),
+                          PROMOTE && (g.ws != nullptr || g.ws_need != nullptr));
       // the un-promoted variant runs at the tensor pipe's rate, where the
       // pair's halved B reads from shared memory matter: the 256 x 256 pair
       // in place of the one-CTA 128 x 256 tile (same waves)

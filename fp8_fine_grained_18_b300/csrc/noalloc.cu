@@ -10,13 +10,13 @@
 namespace fp8bs {
 namespace {
 
-// 32 MiB: room for the stream-K workspace of the tile shapes the automatic
-// choice makes for few-tile problems on 148 SMs (about 19.4 MB for 256x128
-// CTA pairs or 128x128 CTAs); plans that need more (devices with more SMs)
-// are refused by the entry point.  The array is zero when the module loads.  The CUDA runtime places
-// it when this module is loaded: on first use under lazy module loading
-// (the default), at context creation otherwise.
-constexpr size_t kScratchBytes = size_t(32) << 20;
+// 48 MiB: room for every stream-K workspace on 148 SMs (at most about
+// 38.8 MB: two FP32 shares of a 128 x 256 accumulator per CTA, and the
+// arrival counters); plans that need more (devices with more SMs) are
+// refused by the entry point.  The array is zero when the module loads.
+// The CUDA runtime places it when this module is loaded: on first use under
+// lazy module loading (the default), at context creation otherwise.
+constexpr size_t kScratchBytes = size_t(48) << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;

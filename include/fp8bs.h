@@ -228,11 +228,12 @@ fp8bs_status fp8bs_gemm_tiled(const uint8_t *a, const float *sa,
                               fp8bs_stream_t stream);
 
 /*
- * fp8bs_gemm (promoted, every 128 K [P1¶3]) with stream-K scheduling for
- * problems with too few output tiles for the SMs (long K, small M x N):
- * when whole tiles would keep the SMs busy less than 60% of the time, the
- * K-groups of the last two waves' tiles (all tiles, below two waves) are
- * spread evenly over every SM.  A tile split over several SMs is completed by the last
+ * fp8bs_gemm (promoted, every 128 K [P1¶3]) with stream-K scheduling of an
+ * uneven last wave: when the last wave of whole output tiles would leave
+ * the SMs idle for more than about half a wave (few tiles and long K, or
+ * e.g. 3.03 or 6.05 waves), the K-groups of the last two waves' tiles (all
+ * tiles, below two waves) are spread evenly over every SM.  The tile shape
+ * is chosen with that plan in view, so it may differ from fp8bs_gemm's.  A tile split over several SMs is completed by the last
  * of them to finish: each writes its FP32 share of the tile to the
  * workspace, and the last sums the shares in K order (so the result does
  * not depend on which finishes last; it may differ from fp8bs_gemm's by
@@ -288,7 +289,7 @@ fp8bs_status fp8bs_gemm_streamk(const uint8_t *a, const float *sa,
  *     streams, other host threads) race on it.  Order them on one stream or
  *     synchronize between them.
  */
-#define FP8BS_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define FP8BS_NOALLOC_SCRATCH_BYTES (48u << 20)
 fp8bs_status fp8bs_gemm_streamk_noalloc(const uint8_t *a, const float *sa,
                                         const uint8_t *b, const float *sb,
                                         fp8bs_bscale_kind bkind, int64_t M,
