@@ -87,9 +87,9 @@ def test_streamk_sampled(fp8bs, oracle_mod, bkind):
 
 
 def test_streamk_dgrad_runs_whole_tiles(fp8bs, oracle_mod):
-    """The backward workload's input gradient (4096 x 2048 x 7168: 128 pair
-    tiles on 74 pairs, 86% busy) plans no stream-K -- its hand-off costs
-    more than the partial wave -- and runs as fp8bs_gemm."""
+    """The backward workload's input gradient (4096 x 2048 x 7168: 1.73
+    waves of whole tiles) plans no stream-K -- its hand-off costs more than
+    the partial wave -- and runs as fp8bs_gemm."""
     inp = synth.make_inputs("bwd")
     dy, sdy = oracle_mod.quant_act_1x128(inp["dY"])
     _, _, wT, swT = oracle_mod.quant_weight_128x128(inp["W"], transposed=True)
@@ -99,6 +99,40 @@ def test_streamk_dgrad_runs_whole_tiles(fp8bs, oracle_mod):
     c1 = host(fp8bs.gemm_streamk(da, dsa, db, dsb, BLOCK, out_dtype=torch.bfloat16))
     c2 = host(fp8bs.gemm(da, dsa, db, dsb, BLOCK, out_dtype=torch.bfloat16))
     assert np.array_equal(c1.view(np.uint16), c2.view(np.uint16))
+
+
+def _sampled_positions(M, N, count, seed):
+    rng = np.random.default_rng(seed)
+    ms = np.concatenate([rng.integers(0, M, count), [0, M - 1, M - 1, 0]])
+    ns = np.concatenate([rng.integers(0, N, count), [0, N - 1, 0, N - 1]])
+    return ms, ns
+
+
+def test_streamk_uneven_last_wave_full_sampled(fp8bs, oracle_mod):
+    """Large problems whose last wave of whole tiles is nearly empty get a
+    stream-K plan over the last two waves: the weight gradient (7168 x 2048
+    x 4096, per-column B scales: 3.03 waves of 128 x 256 tiles) and the
+    dense projection (4096 x 7168 x 7168, block B scales: 6.05 waves);
+    sampled outputs against the oracle's double sums."""
+    inp = synth.make_inputs("bwd")
+    dyT, sdyT = oracle_mod.quant_act_128x1(inp["dY"])
+    qx, sx = oracle_mod.quant_act_1x128(inp["X"])
+    xT, sxT = oracle_mod.requant_1x128_to_128x1(qx, sx)
+    dense = synth.make_inputs("dense")
+    a, sa = oracle_mod.quant_act_1x128(dense["A"])
+    w, sw = oracle_mod.quant_weight_128x128(dense["B"])
+    for (qa_, sa_, qb_, sb_, bkind, what) in ((dyT, sdyT, xT, sxT, TILE, "wgrad"),
+                                              (a, sa, w, sw, BLOCK, "dense")):
+        M, K = qa_.shape
+        N = qb_.shape[0]
+        need = fp8bs.gemm_streamk_workspace(M, N, K, bkind, torch.float32)
+        assert need > 0, f"{what}: an uneven last wave should plan stream-K"
+        ms, ns = _sampled_positions(M, N, 3000, M + N)
+        ref = oracle_mod.gemm_sampled(qa_, sa_, qb_, sb_, bkind, ms, ns)
+        c = fp8bs.gemm_streamk(dev(qa_), dev(sa_), dev(qb_), dev(sb_), bkind,
+                               out_dtype=torch.float32)
+        idx = (torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda())
+        assert_gemm_f32(host(c[idx]), ref, f"stream-K {what}")
 
 
 def test_streamk_whole_waves_need_no_workspace(fp8bs, oracle_mod):
