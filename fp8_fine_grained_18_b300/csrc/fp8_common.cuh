@@ -176,18 +176,6 @@ __device__ __forceinline__ uint32_t e5m6_of(float y) {
   return e5m6_code(u & 0x7FFFFFFFu, (u >> 20) & 0x800u);
 }
 
-// Exact value of a code: (c & 0x7FF) << 17 read as FP32 is |value| * 2^-112
-// (exponent field in bits 23..27, mantissa in 17..22; code exponent 0 lands
-// as an FP32 subnormal of the right value), and the power-of-two scaling is
-// exact; exponent 31 is Inf (mantissa 0) or NaN.
-__device__ __forceinline__ float e5m6_decode(uint32_t c) {
-  const uint32_t mag = c & 0x7FFu;
-  const float v = __fmul_rn(__uint_as_float(mag << 17), 0x1.0p112f);
-  const uint32_t special = mag == 0x7C0u ? 0x7F800000u : 0x7FC00000u;
-  const uint32_t bits = mag >= 0x7C0u ? special : __float_as_uint(v);
-  return __uint_as_float(bits | ((c & 0x800u) << 20));
-}
-
 // Eight codes -> the 96-bit little-endian stream, as three words.
 __device__ __forceinline__ uint3 e5m6_pack8(const uint32_t* c) {
   return make_uint3(c[0] | (c[1] << 12) | (c[2] << 24),
