@@ -14,9 +14,9 @@
 // warp moves input tiles into a ring of shared-memory stages with 2-D TMA
 // copies (mbarrier full/empty, every wait bounded), while 16 consumer warps
 // turn each stage into codes and scales and store them.  Where a tile's
-// threads must exchange group maxima, the consumers form two teams of 8
-// warps that work on alternate tiles, so one team's barrier waits overlap
-// the other's work.  Tiles are ordered with the K-group fastest, so the CTAs
+// threads must exchange group maxima, the consumers form teams (two of 8
+// warps, or four of 4 for the E4M3 re-tiling) that work on alternate tiles,
+// so one team's barrier waits overlap the others' work.  Tiles are ordered with the K-group fastest, so the CTAs
 // running at one time read one contiguous band of the input.  Q12, Q1E5 and
 // the transposing ops (Q1T and the dual quantizer as Q1TS, Q3 and the E5M6
 // re-tiling as Q3S) are further ops of the same scheme: a team stages its
@@ -762,8 +762,8 @@ __global__ void tensor_scale_finalize_kernel(float* scale_word) {
 
 // ---------------------------------------------------------------------------
 // The transposing quantizers (128x1 tiles written transposed) are ops of the
-// same streaming scheme.  A team of 8 warps turns one input tile into a
-// 128 x 128 tile of output codes (output rows = input columns, 128 tokens
+// same streaming scheme.  A team (8 warps; 4 for the E4M3 re-tiling) turns
+// one input tile into a 128 x 128 tile of output codes (output rows = input columns, 128 tokens
 // each) and its 128 scales; it writes them into a staging buffer in its
 // shared-memory scratch, and one thread stores both with bulk copies (a 2-D
 // tensor store for the codes, a 512-byte copy for the scales).  The staging
