@@ -78,3 +78,15 @@ def test_algorithmic_bytes_per_element():
     assert bench.algorithmic_bytes_q2(M, K, transposed=True) / n == pytest.approx(4 + 8 / 16384)
     assert bench.algorithmic_bytes_dual(M, K) / n == pytest.approx(2 + 2 * (1 + 4 / 128))
     assert bench.algorithmic_bytes_q3(M, K) / n == pytest.approx(2 * (1 + 4 / 128))
+
+
+def test_cpu_legs_sample_whole_b_blocks():
+    """The CPU legs quantize B in 128x128 blocks on a sample of its rows:
+    every sample starts on a block boundary and stays inside B, so the
+    sample's blocks are blocks of the full-size quantization."""
+    sys.path.insert(0, ROOT)
+    import bench
+    N, n_s = 8192, 256
+    for r0 in list(range(0, N, 37)) + [N - 1, N - 8, 0]:
+        b0 = bench._b_rows(N, r0, n_s)
+        assert b0 % 128 == 0 and 0 <= b0 and b0 + n_s <= N, (r0, b0)
