@@ -849,7 +849,7 @@ def profile_kernel(args):
 def _b_rows(N, r0, n_s):
     """First row of a sample of n_s rows of B: whole 128-row blocks, so that
     the block quantizer sees the blocks the full-size quantization has."""
-    return ((r0 // 128) * 128) % (N - n_s + 1)
+    return min((r0 // 128) * 128, ((N - n_s) // 128) * 128)
 
 
 def cpu_baseline(M, N, K, inp, budget_s=20.0):
