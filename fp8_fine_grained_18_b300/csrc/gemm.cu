@@ -214,13 +214,14 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // PW promotion warps (8, 12 or 16) share the tile's columns: each owns 32
-// TMEM lanes (rows) and kCols = BN / (PW / 4) columns.  The promotion warps'
-// own instruction stream bounds the promoted kernel, not the tensor cores
-// and not the TMEM reads: with the MMAs taken out the 256 x 256 pair runs at
-// the same speed, and a 32-column tcgen05.ld completes in about 20 cycles
-// inside the kernel.  Per K-group each promotion thread spends one FP32
-// operation per element with block B scales and two with per-column B
-// scales (fl(p sb) then fma with sa), which is what separates the two.
+// TMEM lanes (rows) and kCols = BN / (PW / 4) columns.  Per K-group each
+// promotion thread spends one FP32 operation per element with block B
+// scales and two with per-column B scales (fl(p sb) then fma with sa).
+// With per-column scales the promotion warps bound the kernel (with the
+// MMAs taken out the 256 x 256 pair runs at the same speed; the MMA issuer
+// waits for the TMEM buffer most of each K-group); with block scales the
+// chain is balanced: the MMA issuer waits in turn for operands, for the
+// buffer and for the tensor pipe.
 template <int BN, bool PAIR, int PW>
 struct Cfg {
   static constexpr int CM = PAIR ? 2 : 1;  // CTAs per cluster
