@@ -338,6 +338,50 @@ struct Q1E5 {
     const GroupScale mine8 = make_scale(mj, pj >= kBf16Inf, true);
     const int64_t col = (int64_t)kb * kGroup + l16 * 8;
     const int64_t row_bytes = (int64_t)p.K / 2 * 3;
+    // one vote: when all four rows' groups of the warp take the fast
+    // quotient for both formats, only s and -1/s are broadcast and no call
+    // tests a flag
+    if (__all_sync(kFull, l16 >= 4 || (mine5.fast && mine8.fast))) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int src = (lane & 16) + i;
+        const float s5 = __shfl_sync(kFull, mine5.s, src);
+        const float n5 = __shfl_sync(kFull, mine5.nr, src);
+        const float2 s52 = make_float2(s5, s5), n52 = make_float2(n5, n5);
+        const int64_t r = (int64_t)rt * kRows + hw + 32 * i;
+        uint32_t c[8];
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 x = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
+          const float2 q0 = ptx::mul2_rn(x, n52);
+          const float2 qn = ptx::fma2_rn(ptx::fma2_rn(q0, s52, x), n52, q0);
+          const uint32_t ux = __float_as_uint(qn.x), uy = __float_as_uint(qn.y);
+          c[2 * k] = e5m6_code_fast(ux & 0x7FFFFFFFu, (~ux >> 20) & 0x800u);
+          c[2 * k + 1] = e5m6_code_fast(uy & 0x7FFFFFFFu, (~uy >> 20) & 0x800u);
+        }
+        if (p.q) {
+          const float s8 = __shfl_sync(kFull, mine8.s, src);
+          const float n8 = __shfl_sync(kFull, mine8.nr, src);
+          const float2 s82 = make_float2(s8, s8), n82 = make_float2(n8, n8);
+          if (r < p.M) {
+            *reinterpret_cast<uint2*>(p.q + r * p.K + col) =
+                make_uint2(codes_bf16x4_fast(v[i].x, v[i].y, s82, n82),
+                           codes_bf16x4_fast(v[i].z, v[i].w, s82, n82));
+            if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine8.s;
+          }
+        }
+        if (r < p.M) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(p.e5 + r * row_bytes + col / 2 * 3);
+          const uint3 pk = e5m6_pack8(c);
+          dst[0] = pk.x;
+          dst[1] = pk.y;
+          dst[2] = pk.z;
+          if (l16 == i) p.s5[(int64_t)kb * p.M + r] = mine5.s;
+        }
+      }
+      return;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const GroupScale g5 = shfl_scale(mine5, (lane & 16) + i);
