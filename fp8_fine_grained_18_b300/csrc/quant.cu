@@ -31,6 +31,8 @@
 // by the hardware E4M3x2 converter.  Groups that hold Inf/NaN, or whose scale
 // is zero or tiny, take the general per-element path with an exact division;
 // all others use the reciprocal-plus-correction quotient of fp8_common.cuh.
+#include <type_traits>
+
 #include "fp8_common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -1286,17 +1288,29 @@ struct Q3S {
       }
     }
     uint32_t o[4][4];
+    // all_fast: every column takes the reciprocal-based quotient (the
+    // per-column test folds away)
+    auto code_pass = [&](auto all_fast) {
 #pragma unroll
-    for (int i = 0; i < 16; i += 4) {
-      const float4 s4 = *reinterpret_cast<const float4*>(srow + i);
-      float x0[4], x1[4], x2[4], x3[4];
-      dq(i, s4.x, x0);
-      dq(i + 1, s4.y, x1);
-      dq(i + 2, s4.z, x2);
-      dq(i + 3, s4.w, x3);
+      for (int i = 0; i < 16; i += 4) {
+        const float4 s4 = *reinterpret_cast<const float4*>(srow + i);
+        float x0[4], x1[4], x2[4], x3[4];
+        dq(i, s4.x, x0);
+        dq(i + 1, s4.y, x1);
+        dq(i + 2, s4.z, x2);
+        dq(i + 3, s4.w, x3);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], g[c]);
-    }
+        for (int c = 0; c < 4; ++c) {
+          GroupScale gc = g[c];
+          if (decltype(all_fast)::value) gc.fast = true;
+          o[c][i >> 2] = codes_f32x4(x0[c], x1[c], x2[c], x3[c], gc);
+        }
+      }
+    };
+    if (g[0].fast && g[1].fast && g[2].fast && g[3].fast)
+      code_pass(std::true_type());
+    else
+      code_pass(std::false_type());
     release_stage(tm.empty, tm.lane);
     // output rows 4 cq + c', chunk = part; lane cq writes column
     // c' = (c + cq / 2) % 4 at step c
