@@ -56,7 +56,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum of `bench.py --kernel gemm`),
 # valid only for the kernel code it was taken on (a fingerprint of gemm.cu,
 # ptx.cuh and fp8_common.cuh without comments); null once the code changed.
-TRAFFIC = {"gemm": {"bytes": 1121049856 + 252686592, "src_sha": "89910534a4fb83bd"}}
+TRAFFIC = {"gemm": {"bytes": 1129979136 + 252557568, "src_sha": "ea21075bfefe1c74"}}
 
 
 def kernel_source_sha():

@@ -157,19 +157,6 @@ __device__ __forceinline__ uint32_t e5m6_code(uint32_t a, uint32_t sign12) {
   return sign12 | (((r >> 23) - 112u) << 6) | ((r >> 17) & 0x3Fu);
 }
 
-// Fast-path code of a finite magnitude `a` known to be <= 65024 (a group's
-// quotient x / s, |x| <= amax): round to 6 mantissa bits with ties to even
-// by integer addition on the FP32 pattern (exponent and mantissa fields are
-// adjacent, so the carry lands in the exponent), rebias by 112 exponent
-// steps (7168 = 112 * 64); below 2^-14 the multiple of 2^-20 comes from
-// adding 2^23 (whose ulp is 1) to y * 2^20 under round-to-nearest-even.
-__device__ __forceinline__ uint32_t e5m6_code_fast(uint32_t a, uint32_t sign12) {
-  const uint32_t norm = ((a + 0xFFFFu + ((a >> 17) & 1u)) >> 17) - 7168u;
-  const uint32_t sub =
-      __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(a), 0x1.0p20f), 0x1.0p23f)) & 0x7Fu;
-  return sign12 | (a < 0x38800000u ? sub : norm);
-}
-
 // Code of y (any FP32 value, the exact-division path).
 __device__ __forceinline__ uint32_t e5m6_of(float y) {
   const uint32_t u = __float_as_uint(y);

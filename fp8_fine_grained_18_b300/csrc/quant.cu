@@ -304,6 +304,23 @@ struct Q1 {
 // codes for the forward GEMM from the same read.  Same tiles and thread
 // layout as Q1; each lane writes its eight 12-bit codes as three words.
 // ---------------------------------------------------------------------------
+
+// Fast-path E5M6 code of a negated quotient q = -x/s with bit pattern ux
+// (finite, |q| <= 65024; the code's sign is the complement of q's).  Normal
+// range: round the FP32 pattern to 6 mantissa bits with ties to even by one
+// integer addition (exponent and mantissa fields are adjacent, so a carry
+// lands in the exponent), which also rebiases the exponent by 112 steps
+// (7168 = 112 * 64, i.e. 7168 << 17 subtracted before the shift; the
+// pattern is at least 113 << 23 there, so nothing wraps).  Below 2^-14 the
+// multiple of 2^-20 comes from one fused multiply-add, |q| * 2^20 + 2^23,
+// whose product is exact and whose sum rounds to nearest even at an ulp of 1.
+__device__ __forceinline__ uint32_t e5m6_code_negq(uint32_t ux) {
+  const uint32_t a = ux & 0x7FFFFFFFu;
+  const uint32_t norm = (a + ((a >> 17) & 1u) + (0xFFFFu - (7168u << 17))) >> 17;
+  const uint32_t sub = __float_as_uint(__fmaf_rn(__uint_as_float(a), 0x1.0p20f, 0x1.0p23f)) & 0x7Fu;
+  return ((~ux >> 20) & 0x800u) | (a < 0x38800000u ? sub : norm);
+}
+
 struct Q1E5 {
   static constexpr int kRows = 128;
   static constexpr int kStageBytes = kRows * 256;
@@ -359,8 +376,8 @@ struct Q1E5 {
           const float2 q0 = ptx::mul2_rn(x, n52);
           const float2 qn = ptx::fma2_rn(ptx::fma2_rn(q0, s52, x), n52, q0);
           const uint32_t ux = __float_as_uint(qn.x), uy = __float_as_uint(qn.y);
-          c[2 * k] = e5m6_code_fast(ux & 0x7FFFFFFFu, (~ux >> 20) & 0x800u);
-          c[2 * k + 1] = e5m6_code_fast(uy & 0x7FFFFFFFu, (~uy >> 20) & 0x800u);
+          c[2 * k] = e5m6_code_negq(ux);
+          c[2 * k + 1] = e5m6_code_negq(uy);
         }
         if (p.q) {
           const float s8 = __shfl_sync(kFull, mine8.s, src);
@@ -396,8 +413,8 @@ struct Q1E5 {
           const float2 qn =
               neg_quotient_1step_x2(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), g5.s, g5.nr);
           const uint32_t ux = __float_as_uint(qn.x), uy = __float_as_uint(qn.y);
-          c[2 * k] = e5m6_code_fast(ux & 0x7FFFFFFFu, (~ux >> 20) & 0x800u);
-          c[2 * k + 1] = e5m6_code_fast(uy & 0x7FFFFFFFu, (~uy >> 20) & 0x800u);
+          c[2 * k] = e5m6_code_negq(ux);
+          c[2 * k + 1] = e5m6_code_negq(uy);
         }
       } else {
 #pragma unroll
