@@ -875,54 +875,83 @@ struct Q1TS {
     const int t = tm.tid;
     const uint32_t* tw = reinterpret_cast<const uint32_t*>(stage);
     const int cp = t & 63, part = t >> 6;
-    const int hw = t >> 4, l16 = t & 15;
     if constexpr (DUAL) {
       // 1x128 tiles first (their registers are free again before the 128x1
-      // pass): half-warp hw owns rows hw + 16 i (i < 8), lane l16 holds 8
-      // consecutive elements of each.  The row maxima reduce two rows to a
-      // shuffle (q1_row_max, rows 4b .. 4b + 3 to lanes 0..3); those lanes
-      // make the scales and leave them, with the packed quotient operands,
-      // in a per-row table that the half-warp reads back.
+      // pass): each group of 8 lanes owns rows g8 + 32 i (i < 4), and lane
+      // l8 holds elements 8 l8 .. 8 l8 + 7 and 64 + 8 l8 .. 64 + 8 l8 + 7 of
+      // each (a warp's 16-byte reads then cover its four rows' halves
+      // without bank conflicts).  The row maxima reduce two rows to a
+      // shuffle over the group's 8 lanes; lane i (< 4) makes row i's scale
+      // and leaves it, with the packed quotient operands, in a per-row
+      // table that the group reads back.
+      const int g8 = t >> 3, l8 = t & 7;
       uint4 v[8];
       const uint4* st = reinterpret_cast<const uint4*>(stage);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = st[(hw + 16 * i) * 16 + l16];
-      uint32_t mj[2], pj[2];
-      q1_row_max(v, l16, mj[0], pj[0]);
-      q1_row_max(v + 4, l16, mj[1], pj[1]);
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = st[(g8 + 32 * i) * 16 + l8];
+        v[2 * i + 1] = st[(g8 + 32 * i) * 16 + 8 + l8];
+      }
+      auto row_max = [&](bool no_nan, uint32_t& m01, uint32_t& m23) {
+        uint32_t a[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t m = 0;
+          const uint32_t ws[8] = {v[2 * i].x,     v[2 * i].y,     v[2 * i].z,     v[2 * i].w,
+                                  v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m = no_nan ? mag_pair_max_no_nan(m, ws[k]) : mag_pair_max(m, ws[k]);
+          a[i] = halves_max(m);
+        }
+        m01 = a[0] | (a[1] << 16);
+        m23 = a[2] | (a[3] << 16);
+#pragma unroll
+        for (int off = 4; off >= 1; off >>= 1) {
+          m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
+          m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
+        }
+      };
+      uint32_t m01, m23;
+      row_max(false, m01, m23);
+      const uint32_t p01 = m01, p23 = m23;
+      if (__any_sync(kFull, pair_has_nan(m01) || pair_has_nan(m23))) row_max(true, m01, m23);
       float4* rs = reinterpret_cast<float4*>(tm.scratch + kOffRowS);
       bool fast = true;
-      if (l16 < 4) {
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          const GroupScale g = make_scale(mj[b], pj[b] >= kBf16Inf, true);
-          const float n = g.fast ? g.nr : 0.0f;
-          const int r = hw + 16 * (4 * b + l16);
-          rs[r] = make_float4(g.s, g.s, n, n);
-          p.s[(int64_t)kb * p.M + m0 + r] = g.s;
-          fast = fast && g.fast;
-        }
+      if (l8 < 4) {
+        const uint32_t mw = l8 < 2 ? m01 : m23, pw = l8 < 2 ? p01 : p23;
+        const uint32_t mj = (l8 & 1) ? (mw >> 16) : (mw & 0xFFFFu);
+        const uint32_t pj = (l8 & 1) ? (pw >> 16) : (pw & 0xFFFFu);
+        const GroupScale g = make_scale(mj, pj >= kBf16Inf, true);
+        const float n = g.fast ? g.nr : 0.0f;
+        const int r = g8 + 32 * l8;
+        rs[r] = make_float4(g.s, g.s, n, n);
+        p.s[(int64_t)kb * p.M + m0 + r] = g.s;
+        fast = g.fast;
       }
       __syncwarp();
-      uint8_t* qrow = p.q + (m0 + hw) * p.K + k0 + l16 * 8;
+      uint8_t* qrow = p.q + (m0 + g8) * p.K + k0 + l8 * 8;
       if (__all_sync(kFull, fast)) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 c = rs[hw + 16 * i];
+        for (int i = 0; i < 4; ++i) {
+          const float4 c = rs[g8 + 32 * i];
           const float2 s2 = make_float2(c.x, c.y), n2 = make_float2(c.z, c.w);
-          *reinterpret_cast<uint2*>(qrow + (int64_t)16 * i * p.K) =
-              make_uint2(codes_bf16x4_fast(v[i].x, v[i].y, s2, n2),
-                         codes_bf16x4_fast(v[i].z, v[i].w, s2, n2));
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 x = v[2 * i + h];
+            *reinterpret_cast<uint2*>(qrow + (int64_t)32 * i * p.K + 64 * h) =
+                make_uint2(codes_bf16x4_fast(x.x, x.y, s2, n2), codes_bf16x4_fast(x.z, x.w, s2, n2));
+          }
         }
       } else {
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
           GroupScale g;
-          g.s = rs[hw + 16 * i].x;
-          g.nr = rs[hw + 16 * i].z;
+          g.s = rs[g8 + 32 * i].x;
+          g.nr = rs[g8 + 32 * i].z;
           g.fast = g.nr != 0.0f;
-          *reinterpret_cast<uint2*>(qrow + (int64_t)16 * i * p.K) =
-              codes_bf16x8(st[(hw + 16 * i) * 16 + l16], g);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<uint2*>(qrow + (int64_t)32 * i * p.K + 64 * h) = codes_bf16x8(v[2 * i + h], g);
         }
       }
     }
