@@ -220,6 +220,41 @@ __device__ __forceinline__ void q1_row_max(const uint4* v, int l16, uint32_t& mj
   pj = (j & 1) ? (pw >> 16) : (pw & 0xFFFFu);
 }
 
+// The same for groups of 8 lanes that own four rows, lane l8 holding two
+// 8-element halves of each (v[2 i], v[2 i + 1] for row i): rows 0, 1 and
+// 2, 3 reduce packed in one word each over the group's three shuffle
+// levels; lane l8 gets row (l8 & 3)'s maxima.
+__device__ __forceinline__ void q1_row_max8(const uint4 (&v)[8], int l8, uint32_t& mj,
+                                            uint32_t& pj) {
+  auto reduce = [&](bool no_nan, uint32_t& m01, uint32_t& m23) {
+    uint32_t a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t ws[8] = {v[2 * i].x,     v[2 * i].y,     v[2 * i].z,     v[2 * i].w,
+                              v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = no_nan ? mag_pair_max_no_nan(m, ws[k]) : mag_pair_max(m, ws[k]);
+      a[i] = halves_max(m);
+    }
+    m01 = a[0] | (a[1] << 16);
+    m23 = a[2] | (a[3] << 16);
+#pragma unroll
+    for (int off = 4; off >= 1; off >>= 1) {
+      m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
+      m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
+    }
+  };
+  uint32_t m01, m23;
+  reduce(false, m01, m23);
+  const uint32_t p01 = m01, p23 = m23;
+  if (__any_sync(kFull, pair_has_nan(m01) || pair_has_nan(m23))) reduce(true, m01, m23);
+  const int j = l8 & 3;
+  const uint32_t mw = j < 2 ? m01 : m23, pw = j < 2 ? p01 : p23;
+  mj = (j & 1) ? (mw >> 16) : (mw & 0xFFFFu);
+  pj = (j & 1) ? (pw >> 16) : (pw & 0xFFFFu);
+}
+
 // ---------------------------------------------------------------------------
 // Q1: 1x128 tiles.  Tile = 128 rows x one K-group (TMA box 128 x 128 bf16,
 // 32 KB).  Half-warp h (0..31) owns rows h, h + 32, h + 64, h + 96 of the
@@ -244,8 +279,8 @@ struct Q1 {
                                const Params& p) {
     ptx::tma_load_2d(dst, map, bar, (tile % p.KB) * kGroup, (tile / p.KB) * kRows);
   }
-  // R rows per half-warp: 4 when all 16 consumer warps share a tile, 8 for
-  // a team of 8 warps (the fused activation + weight launch).
+  // R rows per half-warp (4: all 16 consumer warps share a tile; a team of
+  // 8 warps, in the fused activation + weight launch, takes consume_team8).
   template <int R = 4>
   __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
                                  const Team& tm) {
@@ -292,6 +327,60 @@ struct Q1 {
             *reinterpret_cast<uint2*>(p.q + r * p.K + col) = codes_bf16x8(v[4 * b + i], g);
             if (l16 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
           }
+        }
+      }
+    }
+  }
+  // A team of 8 warps (the fused activation + weight launch): each group of
+  // 8 lanes owns rows g8 + 32 i (i < 4) of the tile and lane l8 elements
+  // 8 l8 .. 8 l8 + 7 and 64 + 8 l8 .. 64 + 8 l8 + 7 of each; lane i (< 4)
+  // of the group makes row i's scale, one per lane (a half-warp per row
+  // would give each scale-making lane two).
+  __device__ static void consume_team8(const uint8_t* stage, int tile, const Params& p,
+                                       const Team& tm) {
+    const int kb = tile % p.KB, rt = tile / p.KB;
+    const int lane = tm.lane;
+    const int g8 = tm.warp * 4 + (lane >> 3), l8 = lane & 7, gbase = lane & ~7;
+    const uint4* st = reinterpret_cast<const uint4*>(stage);
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = st[(g8 + 32 * i) * 16 + l8];
+      v[2 * i + 1] = st[(g8 + 32 * i) * 16 + 8 + l8];
+    }
+    uint32_t mj, pj;
+    q1_row_max8(v, l8, mj, pj);
+    release_stage(tm.empty, lane);
+    const int64_t col = (int64_t)kb * kGroup + l8 * 8;
+    const GroupScale mine = make_scale(mj, pj >= kBf16Inf, true);
+    const float nmine = mine.fast ? mine.nr : 0.0f;
+    if (__all_sync(kFull, l8 >= 4 || mine.fast)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float si = __shfl_sync(kFull, mine.s, gbase + i);
+        const float ni = __shfl_sync(kFull, nmine, gbase + i);
+        const float2 s2 = make_float2(si, si), n2 = make_float2(ni, ni);
+        const int64_t r = (int64_t)rt * kRows + g8 + 32 * i;
+        if (r < p.M) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 x = v[2 * i + h];
+            *reinterpret_cast<uint2*>(p.q + r * p.K + col + 64 * h) =
+                make_uint2(codes_bf16x4_fast(x.x, x.y, s2, n2), codes_bf16x4_fast(x.z, x.w, s2, n2));
+          }
+          if (l8 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const GroupScale g = shfl_scale(mine, gbase + i);
+        const int64_t r = (int64_t)rt * kRows + g8 + 32 * i;
+        if (r < p.M) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<uint2*>(p.q + r * p.K + col + 64 * h) = codes_bf16x8(v[2 * i + h], g);
+          if (l8 == i) p.s[(int64_t)kb * p.M + r] = mine.s;
         }
       }
     }
@@ -730,7 +819,7 @@ struct Q12 {
   __device__ static void consume(const uint8_t* stage, int tile, const Params& p,
                                  const Team& tm) {
     if (tile < p.t1)
-      Q1::consume<8>(stage, tile, p.a, tm);
+      Q1::consume_team8(stage, tile, p.a, tm);
     else
       Q2::consume(stage, tile - p.t1, p.w, tm);
   }
@@ -892,35 +981,11 @@ struct Q1TS {
         v[2 * i] = st[(g8 + 32 * i) * 16 + l8];
         v[2 * i + 1] = st[(g8 + 32 * i) * 16 + 8 + l8];
       }
-      auto row_max = [&](bool no_nan, uint32_t& m01, uint32_t& m23) {
-        uint32_t a[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint32_t m = 0;
-          const uint32_t ws[8] = {v[2 * i].x,     v[2 * i].y,     v[2 * i].z,     v[2 * i].w,
-                                  v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m = no_nan ? mag_pair_max_no_nan(m, ws[k]) : mag_pair_max(m, ws[k]);
-          a[i] = halves_max(m);
-        }
-        m01 = a[0] | (a[1] << 16);
-        m23 = a[2] | (a[3] << 16);
-#pragma unroll
-        for (int off = 4; off >= 1; off >>= 1) {
-          m01 = __vmaxu2(m01, __shfl_xor_sync(kFull, m01, off));
-          m23 = __vmaxu2(m23, __shfl_xor_sync(kFull, m23, off));
-        }
-      };
-      uint32_t m01, m23;
-      row_max(false, m01, m23);
-      const uint32_t p01 = m01, p23 = m23;
-      if (__any_sync(kFull, pair_has_nan(m01) || pair_has_nan(m23))) row_max(true, m01, m23);
+      uint32_t mj, pj;
+      q1_row_max8(v, l8, mj, pj);
       float4* rs = reinterpret_cast<float4*>(tm.scratch + kOffRowS);
       bool fast = true;
       if (l8 < 4) {
-        const uint32_t mw = l8 < 2 ? m01 : m23, pw = l8 < 2 ? p01 : p23;
-        const uint32_t mj = (l8 & 1) ? (mw >> 16) : (mw & 0xFFFFu);
-        const uint32_t pj = (l8 & 1) ? (pw >> 16) : (pw & 0xFFFFu);
         const GroupScale g = make_scale(mj, pj >= kBf16Inf, true);
         const float n = g.fast ? g.nr : 0.0f;
         const int r = g8 + 32 * l8;
